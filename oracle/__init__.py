@@ -1,0 +1,277 @@
+"""CPU oracle for the fused MaxSim operator -- TEST INFRASTRUCTURE ONLY.
+
+Only the test-suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The library's product path never does:
+it shares no code with this oracle, and the oracle never imports the library.
+
+The arithmetic lives in ``oracle.c`` (plain C, binary64 / int64); this module
+only marshals numpy arrays through ctypes.  Each entry point names the passage
+of "FLASH-MAXSIM: IO-Aware Fused Kernels for Late-Interaction Retrieval"
+(arXiv 2605.29517) it follows.
+
+Every function is pinned by CPU tests (``tests/test_oracle_*.py``) against
+closed forms, invariants, brute force and finite differences.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+from ._build import build_oracle, library_path
+
+__all__ = [
+    "decode", "forward_bits", "forward_f64", "forward_i8", "dot_bits",
+    "backward_f64", "build_csr", "DTYPE_CODES",
+]
+
+DTYPE_CODES = {"fp16": 0, "bf16": 1}
+
+_lib = None
+
+_i32p = np.ctypeslib.ndpointer(dtype=np.int32, flags="C_CONTIGUOUS")
+_i64p = np.ctypeslib.ndpointer(dtype=np.int64, flags="C_CONTIGUOUS")
+_u16p = np.ctypeslib.ndpointer(dtype=np.uint16, flags="C_CONTIGUOUS")
+_i8p = np.ctypeslib.ndpointer(dtype=np.int8, flags="C_CONTIGUOUS")
+_f64p = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
+_f32p = np.ctypeslib.ndpointer(dtype=np.float32, flags="C_CONTIGUOUS")
+_vp = ctypes.c_void_p
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        build_oracle()
+    lib = ctypes.CDLL(path)
+    I32, I64, F32, INT = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_int
+    lib.oracle_decode.argtypes = [INT, _u16p, _f64p, I64]
+    lib.oracle_decode.restype = INT
+    lib.oracle_forward_f64.argtypes = [_f64p, _i32p, I32, I32, _f64p, _i32p, I32, I32,
+                                       I64, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.oracle_forward_f64.restype = INT
+    lib.oracle_forward_bits.argtypes = [INT, _u16p, _i32p, I32, I32, _u16p, _i32p, I32, I32,
+                                        I64, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.oracle_forward_bits.restype = INT
+    lib.oracle_dot_bits.argtypes = [INT, _u16p, I32, _u16p, _i32p, I32, I64,
+                                    _i32p, _i32p, _i32p, _i32p, _f64p]
+    lib.oracle_dot_bits.restype = INT
+    lib.oracle_forward_i8.argtypes = [_i8p, _i32p, I32, I32, _i8p, _i32p, I32, I32, F32, F32,
+                                      I64, _vp, _vp, _vp, _vp, _vp]
+    lib.oracle_forward_i8.restype = INT
+    lib.oracle_backward_f64.argtypes = [_f64p, _i32p, _f64p, _i32p, I32, I32, _f64p, _i32p,
+                                        I32, I32, _f64p, _f64p]
+    lib.oracle_backward_f64.restype = INT
+    lib.oracle_build_csr.argtypes = [_i32p, _i32p, I32, I32, _i32p, I32, _i64p, _i64p]
+    lib.oracle_build_csr.restype = I64
+    _lib = lib
+    return lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _pairs(pairs, n_q, n_docs):
+    if pairs is None:
+        qq, bb = np.divmod(np.arange(n_q * n_docs, dtype=np.int64), max(n_docs, 1))
+        return qq.astype(np.int32), bb.astype(np.int32)
+    pairs = np.asarray(pairs, dtype=np.int32).reshape(-1, 2)
+    return np.ascontiguousarray(pairs[:, 0]), np.ascontiguousarray(pairs[:, 1])
+
+
+def decode(dtype: str, bits: np.ndarray) -> np.ndarray:
+    """Exact binary64 value of stored FP16 / BF16 patterns (uint16 array)."""
+    lib = _load()
+    bits = _c(bits, np.uint16)
+    out = np.empty(bits.shape, dtype=np.float64)
+    rc = lib.oracle_decode(DTYPE_CODES[dtype], bits.reshape(-1), out.reshape(-1), bits.size)
+    if rc != 0:
+        raise ValueError("oracle_decode failed")
+    return out
+
+
+def _run_chunks(n_pairs, threads, fn):
+    """Split [0, n_pairs) into contiguous chunks evaluated on a thread pool.
+
+    The C calls release the GIL, so chunks run on separate cores."""
+    threads = max(1, int(threads))
+    if threads == 1 or n_pairs < 2 * threads:
+        fn(0, n_pairs)
+        return
+    step = (n_pairs + threads - 1) // threads
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        futs = [ex.submit(fn, s, min(n_pairs, s + step)) for s in range(0, n_pairs, step)]
+        for f in futs:
+            f.result()
+
+
+def forward_bits(dtype: str, Q_bits, q_lens, D_bits, cu_seqlens, pairs=None,
+                 want_rowmax=False, threads=1):
+    """Flash-MaxSim §1 Eq. (1) on stored FP16/BF16 patterns, in binary64.
+
+    Q_bits: uint16 [n_q, lq_max, dim]; D_bits: uint16 [total_tokens, dim];
+    cu_seqlens: int32 [n_docs + 1].  ``pairs``: optional int array [P, 2] of
+    (q, b); default = every pair in (q, b) row-major order.
+    Returns dict(score [P] f64, argmax [P, lq_max] i32, and when want_rowmax,
+    rowmax [P, lq_max] f64 and gap [P, lq_max] f64 = top-1 minus top-2).
+    """
+    lib = _load()
+    Q_bits = _c(Q_bits, np.uint16)
+    D_bits = _c(D_bits, np.uint16)
+    q_lens = _c(q_lens, np.int32)
+    cu = _c(cu_seqlens, np.int32)
+    n_q, lq_max, dim = Q_bits.shape
+    n_docs = cu.shape[0] - 1
+    pq, pb = _pairs(pairs, n_q, n_docs)
+    P = pq.shape[0]
+    score = np.empty(P, np.float64)
+    argmax = np.empty((P, lq_max), np.int32)
+    rowmax = np.empty((P, lq_max), np.float64) if want_rowmax else None
+    gap = np.empty((P, lq_max), np.float64) if want_rowmax else None
+    code = DTYPE_CODES[dtype]
+
+    def run(s, e):
+        if e <= s:
+            return
+        rc = lib.oracle_forward_bits(
+            code, Q_bits.reshape(-1), q_lens, n_q, lq_max, D_bits.reshape(-1), cu, n_docs, dim,
+            e - s, _ptr(pq[s:e]), _ptr(pb[s:e]), _ptr(score[s:e]), _ptr(argmax[s:e]),
+            _ptr(None if rowmax is None else rowmax[s:e]), _ptr(None if gap is None else gap[s:e]))
+        if rc != 0:
+            raise ValueError(f"oracle_forward_bits failed ({rc})")
+
+    _run_chunks(P, threads, run)
+    out = {"score": score, "argmax": argmax}
+    if want_rowmax:
+        out["rowmax"] = rowmax
+        out["gap"] = gap
+    return out
+
+
+def forward_f64(Q, q_lens, D, cu_seqlens, pairs=None, want_rowmax=False):
+    """Flash-MaxSim §1 Eq. (1) on binary64 inputs (used by the finite-difference
+    and closed-form pins).  Shapes as in forward_bits."""
+    lib = _load()
+    Q = _c(Q, np.float64)
+    D = _c(D, np.float64)
+    q_lens = _c(q_lens, np.int32)
+    cu = _c(cu_seqlens, np.int32)
+    n_q, lq_max, dim = Q.shape
+    n_docs = cu.shape[0] - 1
+    pq, pb = _pairs(pairs, n_q, n_docs)
+    P = pq.shape[0]
+    score = np.empty(P, np.float64)
+    argmax = np.empty((P, lq_max), np.int32)
+    rowmax = np.empty((P, lq_max), np.float64)
+    gap = np.empty((P, lq_max), np.float64)
+    Dflat = D.reshape(-1) if D.size else np.zeros(1, np.float64)
+    rc = lib.oracle_forward_f64(Q.reshape(-1), q_lens, n_q, lq_max, Dflat, cu, n_docs, dim,
+                                P, _ptr(pq), _ptr(pb), _ptr(score), _ptr(argmax),
+                                _ptr(rowmax), _ptr(gap))
+    if rc != 0:
+        raise ValueError(f"oracle_forward_f64 failed ({rc})")
+    out = {"score": score, "argmax": argmax}
+    if want_rowmax:
+        out["rowmax"] = rowmax
+        out["gap"] = gap
+    return out
+
+
+def dot_bits(dtype, Q_bits, D_bits, cu_seqlens, q, b, i, t):
+    """Exact <Q[q,i], D[cu[b]+t]> for arrays of (q, b, i, t)."""
+    lib = _load()
+    Q_bits = _c(Q_bits, np.uint16)
+    D_bits = _c(D_bits, np.uint16)
+    cu = _c(cu_seqlens, np.int32)
+    n_q, lq_max, dim = Q_bits.shape
+    q, b, i, t = (_c(x, np.int32).reshape(-1) for x in (q, b, i, t))
+    out = np.empty(q.shape[0], np.float64)
+    rc = lib.oracle_dot_bits(DTYPE_CODES[dtype], Q_bits.reshape(-1), lq_max, D_bits.reshape(-1),
+                             cu, dim, q.shape[0], q, b, i, t, out)
+    if rc != 0:
+        raise ValueError("oracle_dot_bits failed")
+    return out
+
+
+def forward_i8(Q, q_lens, D, cu_seqlens, q_scale, d_scale, pairs=None, threads=1):
+    """Flash-MaxSim §4.3.1 INT8 x INT8 MaxSim with one scale per tensor:
+    exact int dots, int maxima (lowest t on ties), int64 sum, one scale.
+    Returns dict(raw [P] int64, score [P] f32, argmax [P, lq_max] i32)."""
+    lib = _load()
+    Q = _c(Q, np.int8)
+    D = _c(D, np.int8)
+    q_lens = _c(q_lens, np.int32)
+    cu = _c(cu_seqlens, np.int32)
+    n_q, lq_max, dim = Q.shape
+    n_docs = cu.shape[0] - 1
+    pq, pb = _pairs(pairs, n_q, n_docs)
+    P = pq.shape[0]
+    raw = np.empty(P, np.int64)
+    score = np.empty(P, np.float32)
+    argmax = np.empty((P, lq_max), np.int32)
+    Dflat = D.reshape(-1) if D.size else np.zeros(1, np.int8)
+
+    def run(s, e):
+        if e <= s:
+            return
+        rc = lib.oracle_forward_i8(Q.reshape(-1), q_lens, n_q, lq_max, Dflat, cu, n_docs, dim,
+                                   float(q_scale), float(d_scale), e - s, _ptr(pq[s:e]),
+                                   _ptr(pb[s:e]), _ptr(raw[s:e]), _ptr(score[s:e]),
+                                   _ptr(argmax[s:e]))
+        if rc != 0:
+            raise ValueError(f"oracle_forward_i8 failed ({rc})")
+
+    _run_chunks(P, threads, run)
+    return {"raw": raw, "score": score, "argmax": argmax}
+
+
+def backward_f64(grad, argmax, Q, q_lens, D, cu_seqlens):
+    """Flash-MaxSim §4.2.1 Eqs. (2)-(3) in scatter form, binary64.
+    grad [n_q, n_docs]; argmax [n_q, n_docs, lq_max]; Q [n_q, lq_max, dim]
+    (float64 values); D [total, dim].  Returns (dQ, dD) in float64."""
+    lib = _load()
+    grad = _c(grad, np.float64)
+    argmax = _c(argmax, np.int32)
+    Q = _c(Q, np.float64)
+    D = _c(D, np.float64)
+    q_lens = _c(q_lens, np.int32)
+    cu = _c(cu_seqlens, np.int32)
+    n_q, lq_max, dim = Q.shape
+    n_docs = cu.shape[0] - 1
+    total = int(cu[-1]) if n_docs > 0 else 0
+    dQ = np.empty((n_q, lq_max, dim), np.float64)
+    dD = np.empty((max(total, 1), dim), np.float64)
+    Dflat = D.reshape(-1) if D.size else np.zeros(1, np.float64)
+    rc = lib.oracle_backward_f64(grad.reshape(-1), argmax.reshape(-1), Q.reshape(-1), q_lens,
+                                 n_q, lq_max, Dflat, cu, n_docs, dim,
+                                 dQ.reshape(-1), dD.reshape(-1))
+    if rc != 0:
+        raise ValueError(f"oracle_backward_f64 failed ({rc})")
+    return dQ, dD[:total]
+
+
+def build_csr(argmax, q_lens, cu_seqlens):
+    """Flash-MaxSim §4.2.2 / Alg. 3 step 1: inverse-grid CSR of the argmax map.
+    Returns (row_ptr [total+1] int64, col_idx [nnz] int64)."""
+    lib = _load()
+    argmax = _c(argmax, np.int32)
+    q_lens = _c(q_lens, np.int32)
+    cu = _c(cu_seqlens, np.int32)
+    n_q, n_docs, lq_max = argmax.shape
+    total = int(cu[-1]) if n_docs > 0 else 0
+    row_ptr = np.empty(total + 1, np.int64)
+    col_idx = np.empty(max(1, n_q * n_docs * lq_max), np.int64)
+    nnz = lib.oracle_build_csr(argmax.reshape(-1), q_lens, n_q, lq_max, cu, n_docs,
+                               row_ptr, col_idx)
+    if nnz < 0:
+        raise ValueError(f"oracle_build_csr failed ({nnz})")
+    return row_ptr, col_idx[:nnz]
