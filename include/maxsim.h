@@ -1,0 +1,173 @@
+/*
+ * maxsim.h -- C ABI of the GB300 (sm_103a) fused MaxSim library.
+ *
+ * The operator is late-interaction scoring as defined in "FLASH-MAXSIM:
+ * IO-Aware Fused Kernels for Late-Interaction Retrieval" (arXiv 2605.29517):
+ *
+ *     score(q, b) = sum_{i < q_lens[q]}  max_{t < Ld_b}  <Q[q, i, :], D_b[t, :]>
+ *
+ * (§1 Eq. (1)), computed without materialising the [B, Lq, Ld] similarity
+ * tensor (§4.1, Alg. 2), together with its training backward (§4.2, Eqs. (2)
+ * and (3), Alg. 3), INT8 x INT8 scoring (§4.3.1) and padding-free
+ * variable-length documents (§4.3.2).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All array pointers are DEVICE pointers owned by the caller.  The library
+ *    never allocates, frees or retains memory; scratch space is passed in as
+ *    a caller-owned workspace whose size the matching *_workspace_size()
+ *    call reports.
+ *  - Calls are stream-ordered and asynchronous: they enqueue work on
+ *    `stream` (a cudaStream_t; NULL = the legacy default stream) and return.
+ *    Outputs are valid once the stream has been synchronised.
+ *  - Layouts.  Q: [n_q, lq_max, dim] row-major, query q's valid tokens are
+ *    rows 0 .. q_lens[q]-1 (the rest is padding and is never read as data).
+ *    D: the packed token rows of all documents, [total_d_tokens, dim]
+ *    row-major; document b owns rows cu_seqlens[b] .. cu_seqlens[b+1]-1.
+ *    cu_seqlens: int32 [n_docs + 1], cu_seqlens[0] = 0, non-decreasing,
+ *    cu_seqlens[n_docs] = total_d_tokens.  A dense batch of equal-length
+ *    documents passes cu_seqlens[b] = b * Ld.
+ *  - Q and D must start on a 16-byte boundary.  dim must be 128 (the pages'
+ *    d; other widths return MAXSIM_ERR_UNSUPPORTED).
+ *  - Synchronous return codes report argument errors before anything is
+ *    enqueued.  A device-side failure (a pipeline wait that timed out, an
+ *    out-of-range argmax handed to the backward) sets a device status word
+ *    that maxsim_device_status() reads; the affected outputs are then
+ *    unspecified.
+ *  - Every result is deterministic: the same inputs give the same bits on
+ *    every run (no floating-point atomics anywhere).
+ */
+#ifndef MAXSIM_H_
+#define MAXSIM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MAXSIM_ABI_VERSION 1
+
+typedef enum {
+    MAXSIM_FP16 = 0, /* IEEE binary16 inputs, FP32 accumulation              */
+    MAXSIM_BF16 = 1, /* bfloat16 inputs, FP32 accumulation                   */
+    MAXSIM_INT8 = 2  /* int8 inputs in [-127, 127], exact integer arithmetic */
+} maxsim_dtype_t;
+
+typedef enum {
+    MAXSIM_OK = 0,
+    MAXSIM_ERR_INVALID_ARGUMENT = 1, /* null/misaligned pointer, bad size      */
+    MAXSIM_ERR_UNSUPPORTED = 2,      /* dim != 128, dtype not supported here   */
+    MAXSIM_ERR_WORKSPACE = 3,        /* workspace missing or too small         */
+    MAXSIM_ERR_CUDA = 4,             /* a CUDA runtime/driver call failed      */
+    MAXSIM_ERR_DEVICE = 5            /* the device status word reports a fault */
+} maxsim_status_t;
+
+/* MAXSIM_ABI_VERSION of the loaded library. */
+int32_t maxsim_abi_version(void);
+
+/* Static text for a status code. */
+const char *maxsim_status_string(maxsim_status_t status);
+
+/*
+ * Bytes of workspace maxsim_forward needs for these sizes (0 when none).
+ * Queries longer than 32 tokens keep one partial sum per 32-token chunk
+ * (FP32, or int64 for INT8); INT8 inputs also keep an FP16 copy of Q.
+ */
+size_t maxsim_forward_workspace_size(int32_t n_q, int32_t lq_max, int32_t n_docs,
+                                     int32_t dim, maxsim_dtype_t dtype);
+
+/*
+ * Fused forward: Flash-MaxSim §4.1 (Alg. 2, the online-max recurrence of
+ * §4.1.1, the query-chunk decomposition of §4.1) over packed documents
+ * (§4.3.2), for N_q queries against B documents (the all-pairs regime of
+ * §3.1).  Each document row is read from HBM once for all queries.
+ *
+ *   Q, D        FP16/BF16/INT8 per `dtype`, layouts above.
+ *   q_lens      int32 [n_q], 0 <= q_lens[q] <= lq_max (device).
+ *   cu_seqlens  int32 [n_docs + 1] (device).
+ *   q_scale, d_scale   INT8 only: one symmetric scale per tensor (§4.3.1,
+ *               read per tensor); ignored for FP16/BF16.
+ *   scores      FP32 [n_q, n_docs], written in full.  FP16/BF16: FP32
+ *               tensor-core dot products, FP32 row maxima, a fixed-order
+ *               FP32 sum over query tokens.  INT8: fp32(raw * (s_Q * s_D))
+ *               with the product evaluated in binary64 once.
+ *   raw_scores  INT8 only, optional (may be NULL): int64 [n_q, n_docs], the
+ *               exact sum of the int32 row maxima.
+ *   argmax      optional (may be NULL): int32 [n_q, n_docs, lq_max].  For a
+ *               valid row, the lowest document-local token index attaining
+ *               the row maximum; -1 for padding rows (i >= q_lens[q]) and
+ *               for empty documents.  This is the saved winner map the
+ *               backward consumes (§4.2.2).
+ *   workspace   device scratch of at least maxsim_forward_workspace_size()
+ *               bytes (may be NULL when that size is 0).
+ * Edge cases: a document with no tokens scores -inf (and raw INT64_MIN) for
+ * a query with at least one valid token; a query with q_lens[q] = 0 scores 0.
+ * Returns MAXSIM_OK or an argument error; nothing is enqueued on error.
+ */
+maxsim_status_t maxsim_forward(const void *Q, const int32_t *q_lens, int32_t n_q, int32_t lq_max,
+                               const void *D, const int32_t *cu_seqlens, int32_t n_docs,
+                               int64_t total_d_tokens, int32_t dim, maxsim_dtype_t dtype,
+                               float q_scale, float d_scale,
+                               float *scores, int64_t *raw_scores, int32_t *argmax,
+                               void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of workspace maxsim_backward / maxsim_build_csr need. */
+size_t maxsim_backward_workspace_size(int32_t n_q, int32_t lq_max, int32_t n_docs,
+                                      int64_t total_d_tokens);
+
+/*
+ * Inverse-grid CSR: Flash-MaxSim §4.2.2 (Alg. 3 step 1).  A source is a
+ * flat position s = (q * n_docs + b) * lq_max + i of `argmax` with
+ * i < q_lens[q] and argmax[s] >= 0; it points at destination row
+ * r = cu_seqlens[b] + argmax[s] of the packed D.
+ *   row_ptr  int32 [total_d_tokens + 1]: row_ptr[r] = number of sources whose
+ *            destination is < r (exclusive cumulative bincount).
+ *   col_idx  int32 [number of sources] (at most n_q * n_docs * lq_max):
+ *            sources ordered by destination, ascending s within a row -- the
+ *            order of a stable argsort of the destinations.
+ * Built per document with an atomic-free, deterministic counting sort.
+ * An argmax entry outside [-1, Ld_b) sets the device status word and the
+ * entry is skipped.  Requires n_q * n_docs * lq_max < 2^31.
+ */
+maxsim_status_t maxsim_build_csr(const int32_t *argmax, const int32_t *q_lens, int32_t n_q,
+                                 int32_t lq_max, const int32_t *cu_seqlens, int32_t n_docs,
+                                 int64_t total_d_tokens, int32_t *row_ptr, int32_t *col_idx,
+                                 void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Training backward: Flash-MaxSim §4.2.1 Eqs. (2)-(3) via Alg. 3 -- the
+ * argmax is inverted into the CSR above (kept in `workspace`), then
+ *   dD[r, :]    = sum over the sources s of row r, in CSR order, of
+ *                 grad_scores[q, b] * Q[q, i, :]      (destination-owned,
+ *                 one writer per row, no atomics; §4.2.3)
+ *   dQ[q, i, :] = sum over b ascending of
+ *                 grad_scores[q, b] * D[cu_seqlens[b] + argmax[q, b, i], :]
+ * both accumulated in FP32 in that fixed order.
+ *   grad_scores FP32 [n_q, n_docs];  argmax as produced by maxsim_forward.
+ *   dQ          FP32 [n_q, lq_max, dim], written in full (padding rows 0).
+ *   dD          FP32 [total_d_tokens, dim], written in full (rows nobody
+ *               selected are 0).
+ * dtype: FP16 or BF16 (INT8 returns MAXSIM_ERR_UNSUPPORTED).
+ */
+maxsim_status_t maxsim_backward(const float *grad_scores, const int32_t *argmax,
+                                const void *Q, const int32_t *q_lens, int32_t n_q, int32_t lq_max,
+                                const void *D, const int32_t *cu_seqlens, int32_t n_docs,
+                                int64_t total_d_tokens, int32_t dim, maxsim_dtype_t dtype,
+                                float *dQ, float *dD,
+                                void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Synchronises `stream`, then reads the device status word of the current
+ * device (0 = no fault); `*code` receives the raw word when non-NULL.
+ * When `clear` is non-zero the word is reset to 0.  Returns MAXSIM_OK,
+ * MAXSIM_ERR_DEVICE when the word is non-zero, or MAXSIM_ERR_CUDA.
+ */
+maxsim_status_t maxsim_device_status(void *stream, int32_t clear, int32_t *code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MAXSIM_H_ */

@@ -1,2 +1,244 @@
-"""GB300-native fused MaxSim (late-interaction scoring) -- placeholder, the
-binding is added with the CUDA library."""
+"""GB300-native fused MaxSim (late-interaction scoring).
+
+Python binding of ``libmaxsim.so`` (C ABI in ``include/maxsim.h``).  This
+module only marshals torch tensors into the C calls -- allocating outputs
+and workspaces with torch, passing data pointers and the current CUDA
+stream; every step of the computation runs in the library's CUDA kernels.
+There is no CPU or PyTorch fallback: if the library is not built or no GPU
+is present, the calls raise.
+
+Entry points (same names as the C ABI):
+  maxsim_forward   -- fused forward (FP16/BF16/INT8, dense or packed docs)
+  maxsim_backward  -- dQ, dD from the saved argmax (inverse-grid CSR)
+  maxsim_build_csr -- the inverse-grid CSR itself
+  maxsim_device_status, maxsim_forward_workspace_size,
+  maxsim_backward_workspace_size, maxsim_abi_version
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "load_library", "library_path", "maxsim_forward", "maxsim_backward", "maxsim_build_csr",
+    "maxsim_device_status", "maxsim_forward_workspace_size", "maxsim_backward_workspace_size",
+    "maxsim_abi_version", "MaxSimError", "DTYPE_CODES",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace",
+                4: "cuda error", 5: "device fault"}
+
+
+class MaxSimError(RuntimeError):
+    def __init__(self, fn: str, status: int, message: str):
+        super().__init__(f"{fn}: {message} (status {status})")
+        self.status = status
+
+
+def library_path() -> str:
+    return os.path.join(_PKG, "libmaxsim.so")
+
+
+def load_library():
+    """Load the in-tree ``libmaxsim.so`` (built by ``__graft_entry__.build()``
+    or ``python -m late_interaction_retrieval_maxsim_gb300._build``)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built; run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                             ctypes.c_size_t)
+    lib.maxsim_abi_version.argtypes = []
+    lib.maxsim_abi_version.restype = i32
+    lib.maxsim_status_string.argtypes = [ctypes.c_int]
+    lib.maxsim_status_string.restype = ctypes.c_char_p
+    lib.maxsim_forward_workspace_size.argtypes = [i32, i32, i32, i32, ctypes.c_int]
+    lib.maxsim_forward_workspace_size.restype = sz
+    lib.maxsim_forward.argtypes = [vp, vp, i32, i32, vp, vp, i32, i64, i32, ctypes.c_int, f32, f32,
+                                   vp, vp, vp, vp, sz, vp]
+    lib.maxsim_forward.restype = ctypes.c_int
+    lib.maxsim_backward_workspace_size.argtypes = [i32, i32, i32, i64]
+    lib.maxsim_backward_workspace_size.restype = sz
+    lib.maxsim_build_csr.argtypes = [vp, vp, i32, i32, vp, i32, i64, vp, vp, vp, sz, vp]
+    lib.maxsim_build_csr.restype = ctypes.c_int
+    lib.maxsim_backward.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp, i32, i64, i32, ctypes.c_int,
+                                    vp, vp, vp, sz, vp]
+    lib.maxsim_backward.restype = ctypes.c_int
+    lib.maxsim_device_status.argtypes = [vp, i32, ctypes.POINTER(i32)]
+    lib.maxsim_device_status.restype = ctypes.c_int
+    _LIB = lib
+    return lib
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    codes = {torch.float16: 0, torch.bfloat16: 1, torch.int8: 2}
+    if t.dtype not in codes:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return codes[t.dtype]
+
+
+DTYPE_CODES = {"fp16": 0, "bf16": 1, "int8": 2}
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        msg = load_library().maxsim_status_string(status).decode()
+        raise MaxSimError(fn, status, msg)
+
+
+def _require(t, name, dtype=None, device=None, contiguous=True):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must live on a CUDA device")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def maxsim_abi_version() -> int:
+    return int(load_library().maxsim_abi_version())
+
+
+def maxsim_forward_workspace_size(n_q: int, lq_max: int, n_docs: int, dtype, dim: int = 128) -> int:
+    code = DTYPE_CODES[dtype] if isinstance(dtype, str) else int(dtype)
+    return int(load_library().maxsim_forward_workspace_size(n_q, lq_max, n_docs, dim, code))
+
+
+def maxsim_backward_workspace_size(n_q: int, lq_max: int, n_docs: int, total_d_tokens: int) -> int:
+    return int(load_library().maxsim_backward_workspace_size(n_q, lq_max, n_docs, total_d_tokens))
+
+
+def maxsim_forward(Q, q_lens, D, cu_seqlens, *, with_argmax: bool = True, q_scale: float = 1.0,
+                   d_scale: float = 1.0, scores=None, argmax=None, raw_scores=None, workspace=None,
+                   want_raw: bool = False, stream=None):
+    """Fused MaxSim forward (C: ``maxsim_forward``).
+
+    Q [n_q, lq_max, 128] and D [total, 128] of the same dtype (float16,
+    bfloat16 or int8); q_lens [n_q] and cu_seqlens [n_docs+1] int32 on the
+    same device.  Returns (scores [n_q, n_docs] float32, argmax [n_q, n_docs,
+    lq_max] int32 or None, raw_scores [n_q, n_docs] int64 or None)."""
+    torch = _torch()
+    lib = load_library()
+    _require(Q, "Q")
+    dev = Q.device
+    _require(D, "D", dtype=Q.dtype, device=dev)
+    _require(q_lens, "q_lens", torch.int32, dev)
+    _require(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    if Q.dim() != 3 or D.dim() != 2 or Q.shape[2] != D.shape[1]:
+        raise ValueError("Q must be [n_q, lq_max, dim] and D [total, dim]")
+    n_q, lq_max, dim = Q.shape
+    n_docs = cu_seqlens.numel() - 1
+    total = D.shape[0]
+    code = _dtype_code(Q)
+    if scores is None:
+        scores = torch.empty((n_q, n_docs), dtype=torch.float32, device=dev)
+    if with_argmax and argmax is None:
+        argmax = torch.empty((n_q, n_docs, lq_max), dtype=torch.int32, device=dev)
+    if not with_argmax:
+        argmax = None
+    if code == 2 and want_raw and raw_scores is None:
+        raw_scores = torch.empty((n_q, n_docs), dtype=torch.int64, device=dev)
+    ws_bytes = maxsim_forward_workspace_size(n_q, lq_max, n_docs, code, dim)
+    if ws_bytes and (workspace is None or workspace.numel() < ws_bytes):
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.maxsim_forward(_ptr(Q), _ptr(q_lens), n_q, lq_max, _ptr(D), _ptr(cu_seqlens), n_docs,
+                                total, dim, code, float(q_scale), float(d_scale), _ptr(scores),
+                                _ptr(raw_scores), _ptr(argmax), _ptr(workspace),
+                                workspace.numel() if workspace is not None else 0, _stream(stream))
+    _check("maxsim_forward", st)
+    return scores, argmax, raw_scores
+
+
+def maxsim_build_csr(argmax, q_lens, cu_seqlens, total_d_tokens: int, *, workspace=None, stream=None):
+    """Inverse-grid CSR of an argmax map (C: ``maxsim_build_csr``).
+    Returns (row_ptr [total+1] int32, col_idx [n_sources] int32)."""
+    torch = _torch()
+    lib = load_library()
+    _require(argmax, "argmax", torch.int32)
+    dev = argmax.device
+    _require(q_lens, "q_lens", torch.int32, dev)
+    _require(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    n_q, n_docs, lq_max = argmax.shape
+    row_ptr = torch.empty(total_d_tokens + 1, dtype=torch.int32, device=dev)
+    col_idx = torch.empty(max(1, n_q * n_docs * lq_max), dtype=torch.int32, device=dev)
+    ws_bytes = maxsim_backward_workspace_size(n_q, lq_max, n_docs, total_d_tokens)
+    if workspace is None or workspace.numel() < ws_bytes:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.maxsim_build_csr(_ptr(argmax), _ptr(q_lens), n_q, lq_max, _ptr(cu_seqlens), n_docs,
+                                  total_d_tokens, _ptr(row_ptr), _ptr(col_idx), _ptr(workspace),
+                                  workspace.numel(), _stream(stream))
+    _check("maxsim_build_csr", st)
+    nnz = int(row_ptr[-1].item())
+    return row_ptr, col_idx[:nnz]
+
+
+def maxsim_backward(grad_scores, argmax, Q, q_lens, D, cu_seqlens, *, dQ=None, dD=None,
+                    workspace=None, stream=None):
+    """Backward of the fused MaxSim (C: ``maxsim_backward``).
+    Returns (dQ [n_q, lq_max, 128] float32, dD [total, 128] float32)."""
+    torch = _torch()
+    lib = load_library()
+    _require(Q, "Q")
+    dev = Q.device
+    _require(D, "D", dtype=Q.dtype, device=dev)
+    _require(grad_scores, "grad_scores", torch.float32, dev)
+    _require(argmax, "argmax", torch.int32, dev)
+    _require(q_lens, "q_lens", torch.int32, dev)
+    _require(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    n_q, lq_max, dim = Q.shape
+    n_docs = cu_seqlens.numel() - 1
+    total = D.shape[0]
+    if dQ is None:
+        dQ = torch.empty((n_q, lq_max, dim), dtype=torch.float32, device=dev)
+    if dD is None:
+        dD = torch.empty((total, dim), dtype=torch.float32, device=dev)
+    ws_bytes = maxsim_backward_workspace_size(n_q, lq_max, n_docs, total)
+    if workspace is None or workspace.numel() < ws_bytes:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.maxsim_backward(_ptr(grad_scores), _ptr(argmax), _ptr(Q), _ptr(q_lens), n_q, lq_max,
+                                 _ptr(D), _ptr(cu_seqlens), n_docs, total, dim, _dtype_code(Q),
+                                 _ptr(dQ), _ptr(dD), _ptr(workspace), workspace.numel(),
+                                 _stream(stream))
+    _check("maxsim_backward", st)
+    return dQ, dD
+
+
+def maxsim_device_status(clear: bool = True, stream=None) -> int:
+    """Synchronise the stream and return the device status word (0 = ok)."""
+    lib = load_library()
+    code = ctypes.c_int32(0)
+    st = lib.maxsim_device_status(_stream(stream), 1 if clear else 0, ctypes.byref(code))
+    if st not in (0, 5):
+        _check("maxsim_device_status", st)
+    return int(code.value)

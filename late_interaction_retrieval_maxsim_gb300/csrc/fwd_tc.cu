@@ -1,0 +1,531 @@
+// fwd_tc.cu -- fused MaxSim forward on the sm_103a tensor cores.
+//
+// "FLASH-MAXSIM: IO-Aware Fused Kernels for Late-Interaction Retrieval"
+// (arXiv 2605.29517) §4.1, Alg. 2: stream document tiles, form the
+// similarity sub-tile on chip, fold it into a running row maximum (§4.1.1,
+// masking positions outside the document to -inf before the reduction), and
+// write one scalar per (query, document) pair; padding-free packed documents
+// per §4.3.2; INT8 x INT8 per §4.3.1 (one scale per tensor).
+//
+// GB300 design (differs from the pages' one-program-per-pair scheme):
+//  * One CTA owns up to 4 M-tiles of 128 padded query rows (all queries of a
+//    small batch at once) resident in shared memory, and streams a
+//    token-balanced contiguous range of documents through a TMA pipeline, so
+//    every document row is read from HBM once for all those queries.
+//  * tcgen05.mma (M=128, N=128 tokens, K=16, FP32 accumulate) writes
+//    similarity tiles into TMEM; 4 accumulator slots of 128 columns let the
+//    MMA run ahead of the epilogue.
+//  * Epilogue warps (one warp-set of 4 per M-tile, one thread per query row)
+//    read TMEM with tcgen05.ld and fold each 32-column chunk into the row's
+//    running (max, argmax) with a balanced comparison tree (ties keep the
+//    lowest token), splitting chunks at document boundaries; at a document's
+//    end the warp writes the argmax row and reduces the maxima over query
+//    tokens with a fixed shuffle tree.  Queries longer than 32 tokens leave
+//    one partial per 32-token chunk, summed in chunk order by a second pass.
+//  * INT8: a converter warp-set widens each int8 tile to FP16 in shared
+//    memory (exact: |x| <= 127) for the same FP16 MMA; every product and
+//    partial sum is an integer below 2^24, so the FP32 accumulator holds the
+//    exact int32 dot product, and sums over query tokens run in int64.
+#include "internal.cuh"
+#include "sm103.cuh"
+
+#include <cuda_fp16.h>
+
+namespace maxsim {
+namespace {
+
+using namespace ptx;
+
+constexpr int kBlockN = 128;                   // document tokens per tile (MMA N)
+constexpr int kKBlockBytes = 128 * 128;        // 128 rows x 64 16-bit elements, 128B-swizzled
+constexpr int kTileBytes = 2 * kKBlockBytes;   // 128 rows x 128 16-bit elements
+constexpr int kI8TileBytes = 128 * 128;        // 128 rows x 128 int8
+constexpr int kSlots = 4;                      // TMEM accumulator slots
+constexpr int kSlotCols = 128;
+constexpr int kTmemCols = kSlots * kSlotCols;  // 512: the whole TMEM
+
+struct SharedCtl {
+    uint64_t q_full;
+    uint64_t d_full[4];    // FP16 D stage ready for the MMA
+    uint64_t d_empty[4];   // FP16 D stage consumed by the MMA
+    uint64_t i_full[4];    // INT8 staging tile landed
+    uint64_t i_empty[4];   // INT8 staging tile converted
+    uint64_t t_full[kSlots];
+    uint64_t t_empty[kSlots];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int32_t abort;
+    int32_t b_begin, b_end;
+    int32_t t_begin, t_end;
+};
+
+template <int NMT, bool INT8>
+struct Cfg {
+    static constexpr int kStages = INT8 ? (NMT == 4 ? 2 : 3) : (NMT == 4 ? 3 : 4);
+    static constexpr int kI8Stages = INT8 ? (NMT == 4 ? 2 : 4) : 0;
+    static constexpr int kConvWarps = INT8 ? 4 : 0;
+    static constexpr int kFirstEpiWarp = 2 + kConvWarps;
+    static constexpr int kThreads = 32 * (kFirstEpiWarp + 4 * NMT);
+    static constexpr int kQBytes = NMT * kTileBytes;
+    static constexpr int kDBytes = kStages * kTileBytes;
+    static constexpr int kIBytes = kI8Stages * kI8TileBytes;
+    static constexpr int kSmem = 1024 + kQBytes + kDBytes + kIBytes + (int)sizeof(SharedCtl);
+};
+
+__device__ __forceinline__ int lower_bound_cu(const int32_t *cu, int n, int64_t key) {
+    // first index in [0, n] with cu[index] >= key (cu[n] is the token total)
+    int lo = 0, hi = n;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (static_cast<int64_t>(cu[mid]) >= key) hi = mid; else lo = mid + 1;
+    }
+    return lo;
+}
+
+// Running (max, lowest argmax) update with 32 candidate columns c0 + k.
+// A balanced tree: at every node the right (higher-index) candidate wins
+// only when strictly greater, so equal values keep the lowest index.
+__device__ __forceinline__ void fold_argmax32(const float (&v)[32], int c0, float &m, int &a) {
+    float x[16];
+    int ix[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const bool p = v[2 * k + 1] > v[2 * k];
+        x[k] = p ? v[2 * k + 1] : v[2 * k];
+        ix[k] = 2 * k + (p ? 1 : 0);
+    }
+#pragma unroll
+    for (int w = 8; w >= 1; w >>= 1) {
+#pragma unroll
+        for (int k = 0; k < w; ++k) {
+            const bool p = x[2 * k + 1] > x[2 * k];
+            x[k] = p ? x[2 * k + 1] : x[2 * k];
+            ix[k] = p ? ix[2 * k + 1] : ix[2 * k];
+        }
+    }
+    if (x[0] > m) {   // later columns win only when strictly greater
+        m = x[0];
+        a = c0 + ix[0];
+    }
+}
+
+__device__ __forceinline__ float max32(const float (&v)[32]) {
+    float y[11];
+#pragma unroll
+    for (int k = 0; k < 10; ++k) y[k] = fmax3(v[3 * k], v[3 * k + 1], v[3 * k + 2]);
+    y[10] = fmaxf(v[30], v[31]);
+    const float z0 = fmax3(y[0], y[1], y[2]);
+    const float z1 = fmax3(y[3], y[4], y[5]);
+    const float z2 = fmax3(y[6], y[7], y[8]);
+    const float z3 = fmaxf(y[9], y[10]);
+    return fmaxf(fmax3(z0, z1, z2), z3);
+}
+
+// Columns outside [lo, hi) of the chunk become -inf (never selected).
+__device__ __forceinline__ void mask_outside(float (&v)[32], int lo, int hi) {
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+        if (k < lo || k >= hi) v[k] = -INFINITY;
+}
+
+// int8 x4 -> fp16 x4 exactly: (x ^ 0x80) in the low byte of 1024.0 gives
+// 1024 + x + 128; subtracting 1152 leaves x.
+__device__ __forceinline__ uint2 widen_i8x4(uint32_t w) {
+    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t lo = __byte_perm(u, 0x64646464u, 0x4140);
+    const uint32_t hi = __byte_perm(u, 0x64646464u, 0x4342);
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+    __half2 l = __hsub2(*reinterpret_cast<const __half2 *>(&lo), bias);
+    __half2 h = __hsub2(*reinterpret_cast<const __half2 *>(&hi), bias);
+    return make_uint2(*reinterpret_cast<uint32_t *>(&l), *reinterpret_cast<uint32_t *>(&h));
+}
+
+template <int NMT, bool ARGMAX, bool INT8>
+__global__ void __launch_bounds__(Cfg<NMT, INT8>::kThreads, 1)
+maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmD,
+                  const FwdParams p) {
+    using C = Cfg<NMT, INT8>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    uint8_t *sQ = smem;
+    uint8_t *sD = smem + C::kQBytes;
+    uint8_t *sI = sD + C::kDBytes;
+    SharedCtl *ctl = reinterpret_cast<SharedCtl *>(sI + C::kIBytes);
+    volatile int32_t *abort_flag = &ctl->abort;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int g = blockIdx.x % p.groups;
+    const int part = blockIdx.x / p.groups;
+    const int64_t rows_total = static_cast<int64_t>(p.n_q) * p.lq_pad;
+    const int row0 = g * NMT * 128;
+    const int64_t mt_left = (rows_total - row0 + 127) / 128;
+    const int n_mt = mt_left < NMT ? static_cast<int>(mt_left) : NMT;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&ctl->q_full, 1);
+        for (int s = 0; s < 4; ++s) {
+            mbar_init(&ctl->d_full[s], INT8 ? 128 : 1);
+            mbar_init(&ctl->d_empty[s], 1);
+            mbar_init(&ctl->i_full[s], 1);
+            mbar_init(&ctl->i_empty[s], INT8 ? 128 : 1);
+        }
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(&ctl->t_full[s], 1);
+            mbar_init(&ctl->t_empty[s], 4);
+        }
+        mbar_init(&ctl->mma_done, 1);
+        fence_mbar_init();
+        ctl->abort = 0;
+        // token-balanced contiguous document range of this part
+        const int64_t T = p.total_tokens;
+        const int64_t lo = T * part / p.parts;
+        const int64_t hi = T * (part + 1) / p.parts;
+        const int bb = lower_bound_cu(p.cu_seqlens, p.n_docs, lo);
+        const int be = (part == p.parts - 1) ? p.n_docs : lower_bound_cu(p.cu_seqlens, p.n_docs, hi);
+        ctl->b_begin = bb;
+        ctl->b_end = max(bb, be);
+        ctl->t_begin = p.cu_seqlens[bb];
+        ctl->t_end = p.cu_seqlens[max(bb, be)];
+    }
+    if (warp == 1) {
+        tmem_alloc(&ctl->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const uint32_t tmem_base = ctl->tmem_base;
+    const int b_begin = ctl->b_begin, b_end = ctl->b_end;
+    const int t_begin = ctl->t_begin, t_end = ctl->t_end;
+    const int n_tiles = (t_end - t_begin + kBlockN - 1) / kBlockN;
+    const bool run_pipeline = n_tiles > 0 && n_mt > 0;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0 && run_pipeline) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmD);
+            mbar_arrive_expect_tx(&ctl->q_full, n_mt * 8 * 4096);
+            for (int c = 0; c < 4 * n_mt; ++c) {
+                const int rho0 = row0 + 32 * c;
+                const int qq = rho0 / p.lq_pad;
+                const int i0 = rho0 - qq * p.lq_pad;
+                uint8_t *dst = sQ + (c >> 2) * kTileBytes + (c & 3) * 4096;
+                tma_load_3d(dst, &tmQ, &ctl->q_full, 0, i0, qq);
+                tma_load_3d(dst + kKBlockBytes, &tmQ, &ctl->q_full, 64, i0, qq);
+            }
+            constexpr int kS = INT8 ? C::kI8Stages : C::kStages;
+            int issued = 0;
+            for (int j = 0; j < n_tiles; ++j) {
+                const int s = j % kS;
+                const uint32_t ph = (j / kS) & 1;
+                const int row = t_begin + j * kBlockN;
+                if (INT8) {
+                    if (!mbar_wait(&ctl->i_empty[s], ph ^ 1, abort_flag, p.status, kStatusTimeoutProducer)) break;
+                    mbar_arrive_expect_tx(&ctl->i_full[s], kI8TileBytes);
+                    tma_load_2d(sI + s * kI8TileBytes, &tmD, &ctl->i_full[s], 0, row);
+                } else {
+                    if (!mbar_wait(&ctl->d_empty[s], ph ^ 1, abort_flag, p.status, kStatusTimeoutProducer)) break;
+                    mbar_arrive_expect_tx(&ctl->d_full[s], kTileBytes);
+                    tma_load_2d(sD + s * kTileBytes, &tmD, &ctl->d_full[s], 0, row);
+                    tma_load_2d(sD + s * kTileBytes + kKBlockBytes, &tmD, &ctl->d_full[s], 64, row);
+                }
+                issued = j + 1;
+            }
+            // no TMA copy may still be landing when the CTA exits
+            mbar_wait(&ctl->q_full, 0, nullptr, p.status, kStatusTimeoutDrain);
+            for (int j = max(0, issued - kS); j < issued; ++j)
+                mbar_wait(INT8 ? &ctl->i_full[j % kS] : &ctl->d_full[j % kS], (j / kS) & 1, nullptr,
+                          p.status, kStatusTimeoutDrain);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0 && run_pipeline) {
+            bool ok = mbar_wait(&ctl->q_full, 0, abort_flag, p.status, kStatusTimeoutMma);
+            tc_fence_after();
+            const uint32_t q_base = smem_u32(sQ);
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                const int s = j % C::kStages;
+                if (!mbar_wait(&ctl->d_full[s], (j / C::kStages) & 1, abort_flag, p.status, kStatusTimeoutMma)) break;
+                tc_fence_after();
+                const uint32_t d_base = smem_u32(sD + s * kTileBytes);
+                for (int mt = 0; mt < n_mt; ++mt) {
+                    const int slot = mt + NMT * (j % (kSlots / NMT));
+                    const uint32_t use = j / (kSlots / NMT);
+                    if (!mbar_wait(&ctl->t_empty[slot], (use & 1) ^ 1, abort_flag, p.status, kStatusTimeoutMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_base = q_base + mt * kTileBytes;
+                    const uint32_t d_tmem = tmem_base + slot * kSlotCols;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t koff = (kk >> 2) * kKBlockBytes + (kk & 3) * 32;
+                        mma_f16_ss(d_tmem, desc_sw128_kmajor(a_base + koff),
+                                   desc_sw128_kmajor(d_base + koff), p.idesc, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&ctl->t_full[slot]);
+                }
+                mma_commit(&ctl->d_empty[s]);
+            }
+            // every MMA has finished before TMEM is released
+            mma_commit(&ctl->mma_done);
+            mbar_wait(&ctl->mma_done, 0, nullptr, p.status, kStatusTimeoutDrain);
+        }
+        __syncwarp();
+    } else if (warp < C::kFirstEpiWarp) {
+        // ------------------------------------------------ INT8 -> FP16 widening
+        const int t = threadIdx.x - 64;  // row of the tile, 0..127
+        if constexpr (INT8) if (run_pipeline) {
+            for (int j = 0; j < n_tiles; ++j) {
+                const int si = j % C::kI8Stages;
+                const int sd = j % C::kStages;
+                if (!mbar_wait(&ctl->i_full[si], (j / C::kI8Stages) & 1, abort_flag, p.status, kStatusTimeoutProducer)) break;
+                if (!mbar_wait(&ctl->d_empty[sd], ((j / C::kStages) & 1) ^ 1, abort_flag, p.status, kStatusTimeoutProducer)) break;
+                const uint8_t *src = sI + si * kI8TileBytes + t * 128;
+                uint8_t *dst = sD + sd * kTileBytes + t * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    // 16 int8 at logical chunk c (128B-swizzled by the TMA)
+                    const uint4 w = *reinterpret_cast<const uint4 *>(src + ((c ^ (t & 7)) << 4));
+                    const uint2 e0 = widen_i8x4(w.x), e1 = widen_i8x4(w.y);
+                    const uint2 e2 = widen_i8x4(w.z), e3 = widen_i8x4(w.w);
+                    // 16 halves = logical 16-byte chunks 2(c%4), 2(c%4)+1 of K-block c/4
+                    uint8_t *kb = dst + (c >> 2) * kKBlockBytes;
+                    const int c16 = 2 * (c & 3);
+                    *reinterpret_cast<uint4 *>(kb + ((c16 ^ (t & 7)) << 4)) = make_uint4(e0.x, e0.y, e1.x, e1.y);
+                    *reinterpret_cast<uint4 *>(kb + (((c16 + 1) ^ (t & 7)) << 4)) = make_uint4(e2.x, e2.y, e3.x, e3.y);
+                }
+                fence_proxy_async_smem();   // generic-proxy writes -> visible to the tensor core
+                mbar_arrive(&ctl->i_empty[si]);
+                mbar_arrive(&ctl->d_full[sd]);
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue
+        const int mt = (warp - C::kFirstEpiWarp) >> 2;
+        const int qd = warp & 3;  // TMEM lane quarter this warp may access
+        if (mt < n_mt) {
+            const int rho_warp = row0 + mt * 128 + qd * 32;
+            const bool warp_rows = rho_warp < rows_total;
+            const int rho = rho_warp + lane;
+            const int q = rho / p.lq_pad;
+            const int i = rho - q * p.lq_pad;
+            const bool row_valid = q < p.n_q && i < p.lq_max;
+            const int qlen = (q < p.n_q) ? p.q_lens[q] : 0;
+            const bool active = row_valid && i < qlen;
+            const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
+
+            float m = -INFINITY;
+            int a = -1;
+            int b = b_begin;
+            int doc_lo = t_begin;
+            int doc_hi = (b < b_end) ? p.cu_seqlens[b + 1] : INT32_MAX;
+            bool aborted = false;
+
+            auto finalize = [&]() {
+                if (ARGMAX && row_valid)
+                    p.argmax[(static_cast<int64_t>(q) * p.n_docs + b) * p.lq_max + i] =
+                        (active && a >= 0) ? a - doc_lo : -1;
+                if (INT8) {
+                    const bool empty_doc = doc_hi == doc_lo;
+                    long long c = (active && !empty_doc) ? static_cast<long long>(m) : 0ll;
+                    if (p.lq_pad <= 32) {
+                        for (int off = 1; off < p.lq_pad; off <<= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
+                        if (i == 0 && q < p.n_q) {
+                            const bool neg_inf = empty_doc && qlen > 0;
+                            const int64_t idx = static_cast<int64_t>(q) * p.n_docs + b;
+                            if (p.raw_scores) p.raw_scores[idx] = neg_inf ? INT64_MIN : c;
+                            p.scores[idx] = neg_inf ? -INFINITY
+                                                    : static_cast<float>(static_cast<double>(c) * p.int8_scale);
+                        }
+                    } else {
+                        for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
+                        if (lane == 0 && q < p.n_q)
+                            p.ipartials[(static_cast<int64_t>(i >> 5) * p.n_q + q) * p.n_docs + b] = c;
+                    }
+                } else {
+                    float c = active ? m : 0.0f;
+                    if (p.lq_pad <= 32) {
+                        for (int off = 1; off < p.lq_pad; off <<= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
+                        if (i == 0 && q < p.n_q) p.scores[static_cast<int64_t>(q) * p.n_docs + b] = c;
+                    } else {
+                        for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
+                        if (lane == 0 && q < p.n_q)
+                            p.partials[(static_cast<int64_t>(i >> 5) * p.n_q + q) * p.n_docs + b] = c;
+                    }
+                }
+                m = -INFINITY;
+                a = -1;
+                ++b;
+                doc_lo = doc_hi;
+                doc_hi = (b < b_end) ? p.cu_seqlens[b + 1] : INT32_MAX;
+            };
+
+            for (int j = 0; j < n_tiles; ++j) {
+                const int slot = mt + NMT * (j % (kSlots / NMT));
+                const uint32_t use = j / (kSlots / NMT);
+                if (!mbar_wait(&ctl->t_full[slot], use & 1, abort_flag, p.status, kStatusTimeoutEpilogue)) {
+                    aborted = true;
+                    break;
+                }
+                tc_fence_after();
+                const int tile0 = t_begin + j * kBlockN;
+#pragma unroll
+                for (int kc = 0; kc < 4; ++kc) {
+                    float v[32];
+                    __syncwarp();
+                    if (warp_rows) tmem_ld32(tmem_base + lane_base + slot * kSlotCols + kc * 32, v);
+                    if (kc == 3) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&ctl->t_empty[slot]);
+                    }
+                    if (!warp_rows) continue;
+                    const int c0 = tile0 + kc * 32;
+                    const int cend = min(c0 + 32, t_end);
+                    int c = c0;
+                    while (c < cend) {
+                        while (doc_hi <= c) finalize();
+                        const int seg_end = min(doc_hi, cend);
+                        if (c == c0 && seg_end == c0 + 32) {
+                            if (ARGMAX) fold_argmax32(v, c0, m, a);
+                            else m = fmaxf(m, max32(v));
+                        } else {
+                            float w[32];
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) w[k] = v[k];
+                            mask_outside(w, c - c0, seg_end - c0);
+                            if (ARGMAX) fold_argmax32(w, c0, m, a);
+                            else m = fmaxf(m, max32(w));
+                        }
+                        c = seg_end;
+                    }
+                }
+            }
+            if (!aborted && warp_rows)
+                while (b < b_end) finalize();
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// Sum the per-32-token-chunk partials of queries longer than 32 tokens, in
+// chunk order (the query-chunk decomposition of §4.1).
+__global__ void finalize_partials_kernel(FwdParams p, int n_chunks, bool int8) {
+    const int64_t n_pairs = static_cast<int64_t>(p.n_q) * p.n_docs;
+    for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n_pairs;
+         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        if (int8) {
+            const int q = static_cast<int>(idx / p.n_docs);
+            const int b = static_cast<int>(idx - static_cast<int64_t>(q) * p.n_docs);
+            long long s = 0;
+            for (int c = 0; c < n_chunks; ++c) s += p.ipartials[c * n_pairs + idx];
+            const bool neg_inf = p.cu_seqlens[b + 1] == p.cu_seqlens[b] && p.q_lens[q] > 0;
+            if (p.raw_scores) p.raw_scores[idx] = neg_inf ? INT64_MIN : s;
+            p.scores[idx] = neg_inf ? -INFINITY : static_cast<float>(static_cast<double>(s) * p.int8_scale);
+        } else {
+            float s = 0.0f;
+            for (int c = 0; c < n_chunks; ++c) s += p.partials[c * n_pairs + idx];
+            p.scores[idx] = s;
+        }
+    }
+}
+
+// No document has a token (or no query has a row): every score is an empty
+// maximum (-inf) for a query with tokens, an empty sum (0) otherwise.
+__global__ void fill_empty_kernel(FwdParams p, bool int8) {
+    const int64_t n_pairs = static_cast<int64_t>(p.n_q) * p.n_docs;
+    for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n_pairs;
+         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int q = static_cast<int>(idx / p.n_docs);
+        const bool has = p.q_lens[q] > 0;
+        p.scores[idx] = has ? -INFINITY : 0.0f;
+        if (int8 && p.raw_scores) p.raw_scores[idx] = has ? INT64_MIN : 0;
+        if (p.argmax)
+            for (int i = 0; i < p.lq_max; ++i) p.argmax[idx * p.lq_max + i] = -1;
+    }
+}
+
+__global__ void int8_to_f16_kernel(const int8_t *__restrict__ src, __half *__restrict__ dst, int64_t n) {
+    for (int64_t k = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; k < n;
+         k += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        dst[k] = __int2half_rn(static_cast<int>(src[k]));
+}
+
+template <int NMT, bool ARGMAX, bool INT8>
+cudaError_t launch_one(const CUtensorMap &tmQ, const CUtensorMap &tmD, const FwdParams &p,
+                       cudaStream_t stream) {
+    using C = Cfg<NMT, INT8>;
+    auto kern = maxsim_fwd_kernel<NMT, ARGMAX, INT8>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    kern<<<p.groups * p.parts, C::kThreads, C::kSmem, stream>>>(tmQ, tmD, p);
+    return cudaGetLastError();
+}
+
+template <bool ARGMAX, bool INT8>
+cudaError_t launch_nmt(int nmt, const CUtensorMap &tmQ, const CUtensorMap &tmD, const FwdParams &p,
+                       cudaStream_t stream) {
+    switch (nmt) {
+        case 1: return launch_one<1, ARGMAX, INT8>(tmQ, tmD, p, stream);
+        case 2: return launch_one<2, ARGMAX, INT8>(tmQ, tmD, p, stream);
+        default: return launch_one<4, ARGMAX, INT8>(tmQ, tmD, p, stream);
+    }
+}
+
+int grid_for(int64_t n, int threads) {
+    return static_cast<int>(std::min<int64_t>((n + threads - 1) / threads, 4096));
+}
+
+}  // namespace
+
+int forward_smem_bytes(int nmt, bool int8) {
+    if (int8) return nmt == 1 ? Cfg<1, true>::kSmem : nmt == 2 ? Cfg<2, true>::kSmem : Cfg<4, true>::kSmem;
+    return nmt == 1 ? Cfg<1, false>::kSmem : nmt == 2 ? Cfg<2, false>::kSmem : Cfg<4, false>::kSmem;
+}
+
+int forward_threads(int nmt, bool int8) {
+    if (int8) return nmt == 1 ? Cfg<1, true>::kThreads : nmt == 2 ? Cfg<2, true>::kThreads : Cfg<4, true>::kThreads;
+    return nmt == 1 ? Cfg<1, false>::kThreads : nmt == 2 ? Cfg<2, false>::kThreads : Cfg<4, false>::kThreads;
+}
+
+cudaError_t launch_forward(const CUtensorMap &tmQ, const CUtensorMap &tmD, const FwdParams &p,
+                           int nmt, bool with_argmax, bool int8, cudaStream_t stream) {
+    if (int8)
+        return with_argmax ? launch_nmt<true, true>(nmt, tmQ, tmD, p, stream)
+                           : launch_nmt<false, true>(nmt, tmQ, tmD, p, stream);
+    return with_argmax ? launch_nmt<true, false>(nmt, tmQ, tmD, p, stream)
+                       : launch_nmt<false, false>(nmt, tmQ, tmD, p, stream);
+}
+
+cudaError_t launch_finalize_partials(const FwdParams &p, bool int8, cudaStream_t stream) {
+    const int64_t n = static_cast<int64_t>(p.n_q) * p.n_docs;
+    if (n == 0) return cudaSuccess;
+    finalize_partials_kernel<<<grid_for(n, 256), 256, 0, stream>>>(p, p.lq_pad / 32, int8);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fill_empty(const FwdParams &p, bool int8, cudaStream_t stream) {
+    const int64_t n = static_cast<int64_t>(p.n_q) * p.n_docs;
+    if (n == 0) return cudaSuccess;
+    fill_empty_kernel<<<grid_for(n, 256), 256, 0, stream>>>(p, int8);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_int8_to_f16(const int8_t *src, uint16_t *dst, int64_t n, cudaStream_t stream) {
+    if (n == 0) return cudaSuccess;
+    int8_to_f16_kernel<<<grid_for(n, 256), 256, 0, stream>>>(src, reinterpret_cast<__half *>(dst), n);
+    return cudaGetLastError();
+}
+
+}  // namespace maxsim

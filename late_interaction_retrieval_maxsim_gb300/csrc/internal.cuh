@@ -1,0 +1,65 @@
+// internal.cuh -- declarations shared between the host layer and the kernel
+// translation units of the MaxSim library (not part of the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace maxsim {
+
+// Query rows of all queries are laid out "padded": query q, token i sits at
+// padded row rho = q * lq_pad + i, where lq_pad is lq_max rounded up to a
+// power of two (lq_max <= 32) or to a multiple of 32 (lq_max > 32), so a
+// 32-row warp slice never mixes a query's tokens with another query's
+// unless whole queries share it.
+struct FwdParams {
+    const int32_t *q_lens;
+    const int32_t *cu_seqlens;
+    float *scores;       // [n_q, n_docs]
+    float *partials;     // [lq_pad / 32, n_q, n_docs] when lq_pad > 32
+    int64_t *ipartials;  // INT8: [lq_pad / 32, n_q, n_docs] int64 when lq_pad > 32
+    int64_t *raw_scores; // INT8 only, may be null
+    int32_t *argmax;     // [n_q, n_docs, lq_max] or null
+    int32_t *status;     // device status word
+    int32_t n_q, lq_max, lq_pad, n_docs;
+    int32_t total_tokens;
+    int32_t groups, parts;  // grid = groups * parts CTAs
+    uint32_t idesc;         // tcgen05 instruction descriptor
+    double int8_scale;      // (double)q_scale * (double)d_scale
+};
+
+// Number of 128-row M-tiles one CTA holds (1, 2 or 4) for R padded rows.
+inline int forward_mtiles(int64_t rows) { return rows <= 128 ? 1 : rows <= 256 ? 2 : 4; }
+
+// fwd_tc.cu
+int forward_smem_bytes(int nmt, bool int8);
+int forward_threads(int nmt, bool int8);
+cudaError_t launch_forward(const CUtensorMap &tmQ, const CUtensorMap &tmD, const FwdParams &p,
+                           int nmt, bool with_argmax, bool int8, cudaStream_t stream);
+cudaError_t launch_finalize_partials(const FwdParams &p, bool int8, cudaStream_t stream);
+cudaError_t launch_fill_empty(const FwdParams &p, bool int8, cudaStream_t stream);
+cudaError_t launch_int8_to_f16(const int8_t *src, uint16_t *dst, int64_t n, cudaStream_t stream);
+
+// bwd.cu
+struct BwdParams {
+    const float *grad;       // [n_q, n_docs]
+    const int32_t *argmax;   // [n_q, n_docs, lq_max]
+    const void *Q;           // [n_q, lq_max, 128] fp16/bf16
+    const void *D;           // [total, 128]
+    const int32_t *q_lens;
+    const int32_t *cu_seqlens;
+    float *dQ;               // [n_q, lq_max, 128]
+    float *dD;               // [total, 128]
+    int32_t *row_ptr;        // [total + 1]
+    int32_t *col_idx;        // [n_q * n_docs * lq_max]
+    int32_t *doc_count;      // [n_docs + 1] scratch: sources per document, then offsets
+    int32_t *status;
+    int32_t n_q, lq_max, n_docs, total_tokens;
+    int32_t bf16;
+};
+cudaError_t launch_build_csr(const BwdParams &p, cudaStream_t stream);
+cudaError_t launch_grad_d(const BwdParams &p, cudaStream_t stream);
+cudaError_t launch_grad_q(const BwdParams &p, cudaStream_t stream);
+
+}  // namespace maxsim

@@ -1,0 +1,354 @@
+// maxsim_api.cu -- the C ABI declared in include/maxsim.h: argument checks,
+// TMA descriptor encoding, shape-based configuration and launches.  The
+// library allocates nothing; all scratch comes from caller workspaces.
+#include "maxsim.h"
+
+#include "internal.cuh"
+#include "sm103.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <mutex>
+#include <unordered_map>
+
+namespace maxsim {
+
+// Device status word: 0 = healthy; kernels record a code here on a pipeline
+// timeout or an out-of-range argmax (see sm103.cuh for the codes).
+__device__ int32_t g_status_word = 0;
+
+namespace {
+
+constexpr int kDim = 128;
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct DeviceInfo {
+    int sm_count = 0;
+    int32_t *status = nullptr;
+};
+
+std::mutex g_mu;
+std::unordered_map<int, DeviceInfo> g_devices;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+maxsim_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MAXSIM_OK : MAXSIM_ERR_CUDA; }
+
+maxsim_status_t device_info(DeviceInfo *out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MAXSIM_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    auto it = g_devices.find(dev);
+    if (it == g_devices.end()) {
+        DeviceInfo di;
+        if (cudaDeviceGetAttribute(&di.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return MAXSIM_ERR_CUDA;
+        if (cudaGetSymbolAddress(reinterpret_cast<void **>(&di.status), g_status_word) != cudaSuccess)
+            return MAXSIM_ERR_CUDA;
+        it = g_devices.emplace(dev, di).first;
+    }
+    if (g_encode == nullptr) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return MAXSIM_ERR_CUDA;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    *out = it->second;
+    return MAXSIM_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int lq_padded(int lq_max) {
+    if (lq_max <= 32) {
+        int v = 1;
+        while (v < lq_max) v <<= 1;
+        return v;
+    }
+    return (lq_max + 31) / 32 * 32;
+}
+
+// Rank-3 map over Q [n_q][lq_max][128] (16-bit elements): a box is one
+// 64-column K-block of 32 padded query rows -- 32 tokens of one query, or
+// 32 / lq_pad whole queries of lq_pad tokens; rows past lq_max or n_q read 0.
+maxsim_status_t encode_q(CUtensorMap *map, const void *Q, int n_q, int lq_max, int lq_pad, bool bf16) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(lq_max),
+                          static_cast<cuuint64_t>(n_q)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(kDim) * 2,
+                             static_cast<cuuint64_t>(lq_max) * kDim * 2};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(std::min(32, lq_pad)),
+                         static_cast<cuuint32_t>(std::max(1, 32 / lq_pad))};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                          const_cast<void *>(Q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MAXSIM_OK : MAXSIM_ERR_CUDA;
+}
+
+// Rank-2 map over the packed D [total][128]: 16-bit -> boxes of 64 columns x
+// 128 tokens; int8 -> boxes of 128 columns x 128 tokens.  Rows past the end
+// read 0 and are masked by the kernel.
+maxsim_status_t encode_d(CUtensorMap *map, const void *D, int64_t total, maxsim_dtype_t dtype) {
+    const bool i8 = dtype == MAXSIM_INT8;
+    const cuuint64_t esize = i8 ? 1 : 2;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(total)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDim) * esize};
+    cuuint32_t box[2] = {i8 ? 128u : 64u, 128u};
+    cuuint32_t estr[2] = {1, 1};
+    CUtensorMapDataType t = i8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                               : (dtype == MAXSIM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+    CUresult r = g_encode(map, t, 2, const_cast<void *>(D), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MAXSIM_OK : MAXSIM_ERR_CUDA;
+}
+
+struct FwdLayout {
+    size_t partials = 0;   // bytes of per-chunk partial sums
+    size_t q16 = 0;        // bytes of the FP16 copy of an INT8 Q
+    size_t total = 0;
+};
+
+FwdLayout forward_layout(int32_t n_q, int32_t lq_max, int32_t n_docs, maxsim_dtype_t dtype) {
+    FwdLayout l;
+    if (n_q <= 0 || n_docs <= 0 || lq_max <= 0) return l;
+    const int lq_pad = lq_padded(lq_max);
+    if (lq_pad > 32)
+        l.partials = align_up(static_cast<size_t>(lq_pad / 32) * n_q * n_docs *
+                              (dtype == MAXSIM_INT8 ? sizeof(int64_t) : sizeof(float)));
+    if (dtype == MAXSIM_INT8) l.q16 = align_up(static_cast<size_t>(n_q) * lq_max * kDim * 2);
+    l.total = l.partials + l.q16;
+    return l;
+}
+
+struct BwdLayout {
+    size_t row_ptr = 0, col_idx = 0, doc_count = 0, total = 0;
+};
+
+BwdLayout backward_layout(int32_t n_q, int32_t lq_max, int32_t n_docs, int64_t total) {
+    BwdLayout l;
+    l.row_ptr = align_up(static_cast<size_t>(total + 1) * 4);
+    l.col_idx = align_up(static_cast<size_t>(std::max<int64_t>(1, int64_t(n_q) * n_docs * lq_max)) * 4);
+    l.doc_count = align_up(static_cast<size_t>(n_docs + 1) * 4);
+    l.total = l.row_ptr + l.col_idx + l.doc_count;
+    return l;
+}
+
+}  // namespace
+}  // namespace maxsim
+
+using namespace maxsim;
+
+extern "C" {
+
+int32_t maxsim_abi_version(void) { return MAXSIM_ABI_VERSION; }
+
+const char *maxsim_status_string(maxsim_status_t s) {
+    switch (s) {
+        case MAXSIM_OK: return "ok";
+        case MAXSIM_ERR_INVALID_ARGUMENT: return "invalid argument";
+        case MAXSIM_ERR_UNSUPPORTED: return "unsupported configuration";
+        case MAXSIM_ERR_WORKSPACE: return "workspace missing or too small";
+        case MAXSIM_ERR_CUDA: return "CUDA runtime or driver error";
+        case MAXSIM_ERR_DEVICE: return "device status word reports a fault";
+    }
+    return "unknown status";
+}
+
+size_t maxsim_forward_workspace_size(int32_t n_q, int32_t lq_max, int32_t n_docs, int32_t dim,
+                                     maxsim_dtype_t dtype) {
+    (void)dim;
+    return forward_layout(n_q, lq_max, n_docs, dtype).total;
+}
+
+maxsim_status_t maxsim_forward(const void *Q, const int32_t *q_lens, int32_t n_q, int32_t lq_max,
+                               const void *D, const int32_t *cu_seqlens, int32_t n_docs,
+                               int64_t total_d_tokens, int32_t dim, maxsim_dtype_t dtype,
+                               float q_scale, float d_scale, float *scores, int64_t *raw_scores,
+                               int32_t *argmax, void *workspace, size_t workspace_bytes,
+                               void *stream_) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (dtype != MAXSIM_FP16 && dtype != MAXSIM_BF16 && dtype != MAXSIM_INT8) return MAXSIM_ERR_UNSUPPORTED;
+    if (dim != kDim) return MAXSIM_ERR_UNSUPPORTED;
+    if (n_q < 0 || n_docs < 0 || lq_max < 0 || total_d_tokens < 0) return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (total_d_tokens > INT32_MAX - 256) return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (n_q == 0 || n_docs == 0) return MAXSIM_OK;
+    if (!q_lens || !cu_seqlens || !scores) return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (lq_max > 0 && (!Q || !aligned16(Q))) return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (total_d_tokens > 0 && (!D || !aligned16(D))) return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (dtype == MAXSIM_INT8 && !(q_scale > 0.0f && d_scale > 0.0f)) return MAXSIM_ERR_INVALID_ARGUMENT;
+    const int lq_pad = lq_max > 0 ? lq_padded(lq_max) : 1;
+    const int64_t rows = static_cast<int64_t>(n_q) * lq_pad;
+    if (rows > INT32_MAX / 2 || static_cast<int64_t>(n_q) * n_docs * std::max(1, lq_max) > INT64_MAX / 8)
+        return MAXSIM_ERR_INVALID_ARGUMENT;
+    const FwdLayout wl = forward_layout(n_q, lq_max, n_docs, dtype);
+    if (wl.total > 0 && (workspace == nullptr || workspace_bytes < wl.total)) return MAXSIM_ERR_WORKSPACE;
+
+    DeviceInfo di;
+    maxsim_status_t st = device_info(&di);
+    if (st != MAXSIM_OK) return st;
+
+    const bool int8 = dtype == MAXSIM_INT8;
+    FwdParams p{};
+    p.q_lens = q_lens;
+    p.cu_seqlens = cu_seqlens;
+    p.scores = scores;
+    p.raw_scores = int8 ? raw_scores : nullptr;
+    p.argmax = argmax;
+    p.status = di.status;
+    p.n_q = n_q;
+    p.lq_max = lq_max;
+    p.lq_pad = lq_pad;
+    p.n_docs = n_docs;
+    p.total_tokens = static_cast<int32_t>(total_d_tokens);
+    p.int8_scale = int8 ? static_cast<double>(q_scale) * static_cast<double>(d_scale) : 0.0;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    if (wl.partials) {
+        if (int8) p.ipartials = reinterpret_cast<int64_t *>(ws);
+        else p.partials = reinterpret_cast<float *>(ws);
+    }
+
+    if (total_d_tokens == 0 || lq_max == 0) return cuda_status(launch_fill_empty(p, int8, stream));
+
+    const void *q_src = Q;
+    if (int8) {
+        uint16_t *q16 = reinterpret_cast<uint16_t *>(ws + wl.partials);
+        cudaError_t e = launch_int8_to_f16(static_cast<const int8_t *>(Q), q16,
+                                           static_cast<int64_t>(n_q) * lq_max * kDim, stream);
+        if (e != cudaSuccess) return MAXSIM_ERR_CUDA;
+        q_src = q16;
+    }
+    alignas(64) CUtensorMap tmQ;
+    alignas(64) CUtensorMap tmD;
+    if ((st = encode_q(&tmQ, q_src, n_q, lq_max, lq_pad, dtype == MAXSIM_BF16)) != MAXSIM_OK) return st;
+    if ((st = encode_d(&tmD, D, total_d_tokens, dtype)) != MAXSIM_OK) return st;
+
+    const int nmt = forward_mtiles(rows);
+    const int64_t groups = (rows + nmt * 128 - 1) / (nmt * 128);
+    const int64_t parts = std::max<int64_t>(1, di.sm_count / groups);
+    if (groups * parts > INT32_MAX) return MAXSIM_ERR_INVALID_ARGUMENT;
+    p.groups = static_cast<int32_t>(groups);
+    p.parts = static_cast<int32_t>(parts);
+    p.idesc = ptx::idesc_f16(dtype == MAXSIM_BF16, 128, 128);
+
+    cudaError_t e = launch_forward(tmQ, tmD, p, nmt, argmax != nullptr, int8, stream);
+    if (e != cudaSuccess) return MAXSIM_ERR_CUDA;
+    if (lq_pad > 32) {
+        e = launch_finalize_partials(p, int8, stream);
+        if (e != cudaSuccess) return MAXSIM_ERR_CUDA;
+    }
+    return MAXSIM_OK;
+}
+
+size_t maxsim_backward_workspace_size(int32_t n_q, int32_t lq_max, int32_t n_docs, int64_t total_d_tokens) {
+    if (n_q < 0 || lq_max < 0 || n_docs < 0 || total_d_tokens < 0) return 0;
+    return backward_layout(n_q, lq_max, n_docs, total_d_tokens).total;
+}
+
+static maxsim_status_t check_csr_args(const int32_t *argmax, const int32_t *q_lens, int32_t n_q, int32_t lq_max,
+                                      const int32_t *cu_seqlens, int32_t n_docs, int64_t total) {
+    if (n_q < 0 || lq_max < 0 || n_docs < 0 || total < 0 || total > INT32_MAX - 256)
+        return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (static_cast<int64_t>(n_q) * n_docs * lq_max >= INT32_MAX) return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (n_q > 0 && n_docs > 0 && lq_max > 0 && (!argmax || !q_lens)) return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (n_docs > 0 && !cu_seqlens) return MAXSIM_ERR_INVALID_ARGUMENT;
+    return MAXSIM_OK;
+}
+
+static void fill_bwd_params(BwdParams &p, const int32_t *argmax, const int32_t *q_lens, int32_t n_q,
+                            int32_t lq_max, const int32_t *cu_seqlens, int32_t n_docs, int64_t total,
+                            void *workspace, const DeviceInfo &di) {
+    const BwdLayout l = backward_layout(n_q, lq_max, n_docs, total);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    p.argmax = argmax;
+    p.q_lens = q_lens;
+    p.cu_seqlens = cu_seqlens;
+    p.n_q = n_q;
+    p.lq_max = lq_max;
+    p.n_docs = n_docs;
+    p.total_tokens = static_cast<int32_t>(total);
+    p.row_ptr = reinterpret_cast<int32_t *>(ws);
+    p.col_idx = reinterpret_cast<int32_t *>(ws + l.row_ptr);
+    p.doc_count = reinterpret_cast<int32_t *>(ws + l.row_ptr + l.col_idx);
+    p.status = di.status;
+}
+
+maxsim_status_t maxsim_build_csr(const int32_t *argmax, const int32_t *q_lens, int32_t n_q, int32_t lq_max,
+                                 const int32_t *cu_seqlens, int32_t n_docs, int64_t total_d_tokens,
+                                 int32_t *row_ptr, int32_t *col_idx, void *workspace,
+                                 size_t workspace_bytes, void *stream_) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    maxsim_status_t st = check_csr_args(argmax, q_lens, n_q, lq_max, cu_seqlens, n_docs, total_d_tokens);
+    if (st != MAXSIM_OK) return st;
+    if (!row_ptr || !col_idx) return MAXSIM_ERR_INVALID_ARGUMENT;
+    const BwdLayout l = backward_layout(n_q, lq_max, n_docs, total_d_tokens);
+    if (!workspace || workspace_bytes < l.total) return MAXSIM_ERR_WORKSPACE;
+    DeviceInfo di;
+    if ((st = device_info(&di)) != MAXSIM_OK) return st;
+    BwdParams p{};
+    fill_bwd_params(p, argmax, q_lens, n_q, lq_max, cu_seqlens, n_docs, total_d_tokens, workspace, di);
+    p.row_ptr = row_ptr;
+    p.col_idx = col_idx;
+    return cuda_status(launch_build_csr(p, stream));
+}
+
+maxsim_status_t maxsim_backward(const float *grad_scores, const int32_t *argmax, const void *Q,
+                                const int32_t *q_lens, int32_t n_q, int32_t lq_max, const void *D,
+                                const int32_t *cu_seqlens, int32_t n_docs, int64_t total_d_tokens,
+                                int32_t dim, maxsim_dtype_t dtype, float *dQ, float *dD, void *workspace,
+                                size_t workspace_bytes, void *stream_) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (dtype == MAXSIM_INT8) return MAXSIM_ERR_UNSUPPORTED;
+    if (dtype != MAXSIM_FP16 && dtype != MAXSIM_BF16) return MAXSIM_ERR_UNSUPPORTED;
+    if (dim != kDim) return MAXSIM_ERR_UNSUPPORTED;
+    maxsim_status_t st = check_csr_args(argmax, q_lens, n_q, lq_max, cu_seqlens, n_docs, total_d_tokens);
+    if (st != MAXSIM_OK) return st;
+    if ((n_q > 0 && lq_max > 0 && (!dQ || !Q)) || (total_d_tokens > 0 && (!dD || !D)))
+        return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (n_q > 0 && n_docs > 0 && !grad_scores) return MAXSIM_ERR_INVALID_ARGUMENT;
+    const BwdLayout l = backward_layout(n_q, lq_max, n_docs, total_d_tokens);
+    if (!workspace || workspace_bytes < l.total) return MAXSIM_ERR_WORKSPACE;
+    DeviceInfo di;
+    if ((st = device_info(&di)) != MAXSIM_OK) return st;
+    BwdParams p{};
+    fill_bwd_params(p, argmax, q_lens, n_q, lq_max, cu_seqlens, n_docs, total_d_tokens, workspace, di);
+    p.grad = grad_scores;
+    p.Q = Q;
+    p.D = D;
+    p.dQ = dQ;
+    p.dD = dD;
+    p.bf16 = dtype == MAXSIM_BF16;
+    cudaError_t e = launch_build_csr(p, stream);
+    if (e == cudaSuccess) e = launch_grad_d(p, stream);
+    if (e == cudaSuccess) e = launch_grad_q(p, stream);
+    return cuda_status(e);
+}
+
+maxsim_status_t maxsim_device_status(void *stream_, int32_t clear, int32_t *code) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    int32_t v = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_status_word, sizeof v, 0, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return MAXSIM_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return MAXSIM_ERR_CUDA;
+    if (clear && v != 0) {
+        const int32_t zero = 0;
+        if (cudaMemcpyToSymbolAsync(g_status_word, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, stream) !=
+                cudaSuccess ||
+            cudaStreamSynchronize(stream) != cudaSuccess)
+            return MAXSIM_ERR_CUDA;
+    }
+    if (code) *code = v;
+    return v == 0 ? MAXSIM_OK : MAXSIM_ERR_DEVICE;
+}
+
+}  // extern "C"
