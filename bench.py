@@ -1,0 +1,423 @@
+"""Benchmark of the fused MaxSim hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One *step* is one fused forward (scores + the saved argmax) of 16 queries
+(Lq = 32) against a 50,000-document ColBERT-shaped corpus with Ld uniform in
+[32, 300], packed with cu_seqlens, FP16 (the padding-free rerank of
+"FLASH-MAXSIM: IO-Aware Fused Kernels for Late-Interaction Retrieval",
+§4.3.2).  The metric is documents scored per second (each document against
+all 16 queries).  Inputs are seeded synthetic unit-norm embeddings (no
+dataset is read) and exceed L2 (2.1 GB of documents vs a 129 MB L2), so
+every step streams them from HBM.
+
+Under torchrun (N > 1) every rank scores its own 50,000-document shard (weak
+scaling; no collective on the data path, only the timing barrier and max).
+
+Rank 0 prints ONE JSON line.  Besides the contract keys it carries:
+  roofline      the forward kernel's achieved tensor throughput (algorithmic
+                FLOPs / its CUDA-event duration) against the measured peak,
+  cpu_baseline  the CPU oracle timed on the host cores on a bounded sample,
+  e2e           the same metric with host-resident inputs copied in and the
+                scores copied back every step,
+  clocks        SM clocks sampled by nvidia-smi during the timed region,
+  extra         the other workloads (ColPali, training fwd+bwd, INT8).
+
+``--impl reference`` times the CPU oracle (the only reference this method
+has) on the same workload, metric and unit.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "docs scored/s"
+UNIT = "docs/s"
+WORKLOAD = "colbert_varlen"
+L2_BYTES = 129 * 2**20
+
+
+def _dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def _traffic(kernel_file: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, when it was taken
+    on the current kernel source (else None)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path)).get(workload)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "late_interaction_retrieval_maxsim_gb300", "csrc", kernel_file)
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return rec["dram_bytes_per_launch"] if rec.get("source_sha256_16") == h else None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons (background)."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------- ours
+
+def _time_loop(fn, steps, warmup, stream):
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s, e in ev:
+        s.record(stream)
+        fn()
+        e.record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    per = [s.elapsed_time(e) for s, e in ev]
+    return t0.elapsed_time(t1), per
+
+
+def _forward_launches(lq_max: int, int8: bool) -> int:
+    lq_pad = 1 << max(0, (lq_max - 1).bit_length()) if lq_max <= 32 else -(-lq_max // 32) * 32
+    return 1 + (1 if lq_pad > 32 else 0) + (1 if int8 else 0)
+
+
+def _extra_workloads(m, syn, rl, peaks):
+    """Shorter timings of the other workloads (median of 20 CUDA-event reps)."""
+    import torch
+    out = {}
+    stream = torch.cuda.current_stream()
+    for name in ("colpali", "train", "int8_varlen"):
+        w = syn.WORKLOADS[name]
+        x = syn.make_inputs(w, device="cuda")
+        Q, ql, D, cu = x["Q"], x["q_lens"], x["D"], x["cu_seqlens"]
+        kw = dict(q_scale=x["q_scale"], d_scale=x["d_scale"])
+        s, a, _ = m.maxsim_forward(Q, ql, D, cu, **kw)
+        ws = torch.empty(max(1, m.maxsim_forward_workspace_size(w.n_q, w.lq, w.n_docs, w.dtype)),
+                         dtype=torch.uint8, device="cuda")
+        _, per = _time_loop(lambda: m.maxsim_forward(Q, ql, D, cu, scores=s, argmax=a, workspace=ws,
+                                                     **kw), 20, 3, stream)
+        ms = statistics.median(per)
+        flops = rl.forward_flops(int(ql.sum()), D.shape[0])
+        rec = {"n_q": w.n_q, "lq": w.lq, "n_docs": w.n_docs, "ld": [w.ld_lo, w.ld_hi],
+               "dtype": w.dtype, "fwd_ms": round(ms, 4), "docs_per_s": w.n_docs / (ms / 1e3),
+               "fwd_tflops": flops / (ms / 1e3) / 1e12,
+               "fwd_frac_of_measured_bf16_peak": flops / (ms / 1e3) / 1e12 / peaks["bf16_tflops"]}
+        if name == "train":
+            n = s.shape[0]
+            g = torch.softmax(s / 0.05, dim=1)
+            g[torch.arange(n), torch.arange(n)] -= 1.0
+            g = g.contiguous()
+            bws = torch.empty(m.maxsim_backward_workspace_size(w.n_q, w.lq, w.n_docs, D.shape[0]),
+                              dtype=torch.uint8, device="cuda")
+            dq, dd = m.maxsim_backward(g, a, Q, ql, D, cu, workspace=bws)
+            _, perb = _time_loop(lambda: m.maxsim_backward(g, a, Q, ql, D, cu, dQ=dq, dD=dd,
+                                                           workspace=bws), 20, 3, stream)
+            msb = statistics.median(perb)
+            bb = rl.backward_hbm_bytes(w.n_q, w.lq, w.n_docs, D.shape[0], int(ql.sum()) * w.n_docs)
+            rec.update(bwd_ms=round(msb, 4), step_ms=round(ms + msb, 4),
+                       bwd_algorithmic_bytes=bb["total"],
+                       bwd_gbs=bb["total"] / (msb / 1e3) / 1e9,
+                       bwd_frac_of_measured_hbm=bb["total"] / (msb / 1e3) / 1e9 / peaks["hbm_gbs"])
+        if m.maxsim_device_status() != 0:
+            rec["device_status"] = "fault"
+        out[name] = rec
+        del x, Q, D, s, a
+        torch.cuda.empty_cache()
+    return out
+
+
+def _cpu_baseline(x, budget_s=15.0, threads=None):
+    """The oracle, as it stands, on a bounded sample: the 16 queries against a
+    prefix of the documents, on all host cores (one oracle call per chunk of
+    pairs on a thread pool; the C code releases the GIL)."""
+    import numpy as np
+
+    import oracle
+    from late_interaction_retrieval_maxsim_gb300 import synthetic as syn
+    threads = threads or (os.cpu_count() or 1)
+    Q, ql, D, cu = x["Q"], x["q_lens"], x["D"], x["cu_seqlens"]
+    cu_h = cu.cpu().numpy()
+    qb = syn.bits_u16(Q)
+    ql_h = ql.cpu().numpy()
+
+    def run(n_docs):
+        Db = syn.bits_u16(D[: int(cu_h[n_docs])])
+        t = time.perf_counter()
+        oracle.forward_bits("fp16", qb, ql_h, Db, cu_h[: n_docs + 1], threads=threads)
+        return time.perf_counter() - t
+
+    n = 8
+    dt = run(n)
+    while dt < 1.0 and n < 4096:
+        n *= 4
+        dt = run(n)
+    n = max(8, min(int(n * budget_s / max(dt, 1e-3)), 20000))
+    dt = run(n)
+    return {"value": n / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"16 queries x the first {n} of the 50,000 documents ({int(cu_h[n])} tokens), "
+                      f"{dt:.1f} s"}
+
+
+def run_ours(args):
+    import torch
+
+    import late_interaction_retrieval_maxsim_gb300 as m
+    from late_interaction_retrieval_maxsim_gb300 import roofline as rl
+    from late_interaction_retrieval_maxsim_gb300 import synthetic as syn
+
+    world, rank, local = _dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    m.load_library()
+    peaks = _peaks()
+    w = syn.WORKLOADS[WORKLOAD]
+    w = syn.Workload(w.name, w.n_q, w.lq, w.n_docs, w.ld_lo, w.ld_hi, w.dtype, seed=w.seed + rank)
+    x = syn.make_inputs(w, device="cuda")
+    Q, ql, D, cu = x["Q"], x["q_lens"], x["D"], x["cu_seqlens"]
+    total = D.shape[0]
+    scores = torch.empty((w.n_q, w.n_docs), dtype=torch.float32, device="cuda")
+    argmax = torch.empty((w.n_q, w.n_docs, w.lq), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        m.maxsim_forward(Q, ql, D, cu, scores=scores, argmax=argmax)
+
+    step()
+    torch.cuda.synchronize()
+    if m.maxsim_device_status() != 0:
+        raise RuntimeError("device status word set after the first forward")
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        total_ms, per = _time_loop(step, args.steps, args.warmup, stream)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    if m.maxsim_device_status() != 0:
+        raise RuntimeError("device status word set during the timed region")
+
+    ms_per_step = total_ms / args.steps
+    value = w.n_docs * world / (ms_per_step / 1e3)
+    flops = rl.forward_flops(int(ql.sum()), total)
+    kern_ms = statistics.mean(per)
+    achieved = flops / (kern_ms / 1e3) / 1e12
+    roof = {"bound": "tensor", "kernel": "maxsim_fwd_kernel", "achieved": achieved,
+            "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+            "peak_source": f"{peaks['source']} bf16 burst (FP16 runs at the same dense rate)",
+            "algorithmic_flops_per_launch": flops,
+            "traffic": _traffic("fwd_tc.cu", WORKLOAD),
+            "algorithmic_bytes_per_launch": rl.forward_hbm_bytes(w.n_q, w.lq, w.n_docs, total)}
+
+    # end to end through the public API with host-resident inputs
+    Qh = Q.cpu().pin_memory()
+    Dh = D.cpu().pin_memory()
+    qlh = ql.cpu().pin_memory()
+    cuh = cu.cpu().pin_memory()
+    sh = torch.empty(scores.shape, dtype=torch.float32).pin_memory()
+    Qd, Dd, qld, cud = (torch.empty_like(t, device="cuda") for t in (Qh, Dh, qlh, cuh))
+
+    def e2e_step():
+        Qd.copy_(Qh, non_blocking=True)
+        Dd.copy_(Dh, non_blocking=True)
+        qld.copy_(qlh, non_blocking=True)
+        cud.copy_(cuh, non_blocking=True)
+        m.maxsim_forward(Qd, qld, Dd, cud, scores=scores, argmax=argmax)
+        sh.copy_(scores, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    e2e_ms, _ = _time_loop(e2e_step, e2e_steps, 2, stream)
+    h2d = sum(t.numel() * t.element_size() for t in (Qh, Dh, qlh, cuh))
+    d2h = sh.numel() * sh.element_size()
+    e2e = {"value": w.n_docs / (e2e_ms / e2e_steps / 1e3), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+           "path": "pinned host -> device copies, maxsim_forward, scores -> pinned host"}
+    del Qd, Dd
+
+    extra = {}
+    cpu = None
+    if rank == 0 and world == 1:
+        if not args.no_extra:
+            extra = _extra_workloads(m, syn, rl, peaks)
+        cpu = _cpu_baseline(x, budget_s=args.cpu_budget)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp16",
+            "data": "synthetic: seeded N(0,1) token embeddings, L2-normalised, stored FP16",
+            "config": {"workload": WORKLOAD, "n_q": w.n_q, "lq": w.lq, "n_docs_per_gpu": w.n_docs,
+                       "ld": f"U[{w.ld_lo},{w.ld_hi}]", "total_tokens_per_gpu": total, "dim": 128,
+                       "argmax": True,
+                       "l2": f"inputs larger than L2 ({D.numel() * 2 / 1e9:.2f} GB of documents vs "
+                             f"{L2_BYTES / 2**20:.0f} MiB L2), no flush needed",
+                       "parallelism": f"doc-sharded x{world}" if world > 1 else "single GPU"},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps * _forward_launches(w.lq, False),
+            "clocks": clk.summary(),
+            "extra": extra,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- reference
+
+def run_reference(args):
+    """The CPU oracle on the same workload: each step scores the 16 queries
+    against a bounded block of documents (cycling through the corpus)."""
+    world, rank, _ = _dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+
+    import oracle
+    from late_interaction_retrieval_maxsim_gb300 import synthetic as syn
+    w = syn.WORKLOADS[WORKLOAD]
+    threads = os.cpu_count() or 1
+    block = args.ref_docs
+    n_blocks = 8
+    x = syn.make_inputs(w, device="cpu", n_docs=block * n_blocks)
+    qb = syn.bits_u16(x["Q"])
+    ql = x["q_lens"].numpy()
+    cu = x["cu_seqlens"].numpy()
+    Db = syn.bits_u16(x["D"])
+    blocks = []
+    for k in range(n_blocks):
+        lo, hi = int(cu[k * block]), int(cu[(k + 1) * block])
+        blocks.append((Db[lo:hi], (cu[k * block:(k + 1) * block + 1] - lo).astype(np.int32)))
+
+    def step(k):
+        d, c = blocks[k % n_blocks]
+        oracle.forward_bits("fp16", qb, ql, d, c, threads=threads)
+
+    for k in range(args.warmup):
+        step(k)
+    t = time.perf_counter()
+    for k in range(args.steps):
+        step(k)
+    dt = time.perf_counter() - t
+    ms = dt / args.steps * 1e3
+    value = block / (ms / 1e3)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic: seeded N(0,1) token embeddings, L2-normalised, stored FP16",
+            "config": {"workload": WORKLOAD, "n_q": w.n_q, "lq": w.lq, "docs_per_step": block,
+                       "ld": f"U[{w.ld_lo},{w.ld_hi}]", "dim": 128},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": f"{block} documents per step x 16 queries, cycling over "
+                                       f"the first {block * n_blocks} documents"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "torch": torch.__version__}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
+    ap.add_argument("--ref-docs", type=int, default=32, help="documents per reference step")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
