@@ -130,11 +130,13 @@ class ClockSampler:
 
 # --------------------------------------------------------------------- ours
 
-def _time_loop(fn, steps, warmup, stream):
+def _time_loop(fn, steps, warmup, stream, nvtx=None):
     import torch
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
+    if nvtx:
+        torch.cuda.nvtx.range_push(nvtx)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
     t0 = torch.cuda.Event(enable_timing=True)
@@ -146,6 +148,8 @@ def _time_loop(fn, steps, warmup, stream):
         e.record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
+    if nvtx:
+        torch.cuda.nvtx.range_pop()
     per = [s.elapsed_time(e) for s, e in ev]
     return t0.elapsed_time(t1), per
 
@@ -268,7 +272,7 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        total_ms, per = _time_loop(step, args.steps, args.warmup, stream)
+        total_ms, per = _time_loop(step, args.steps, args.warmup, stream, nvtx="timed")
     if world > 1:
         import torch.distributed as dist
         t = torch.tensor([total_ms], device="cuda")

@@ -44,12 +44,14 @@ constexpr int kSlots = 4;                      // TMEM accumulator slots
 constexpr int kSlotCols = 128;
 constexpr int kTmemCols = kSlots * kSlotCols;  // 512: the whole TMEM
 
+constexpr int kMaxStages = 4;
+
 struct SharedCtl {
     uint64_t q_full;
-    uint64_t d_full[4];    // FP16 D stage ready for the MMA
-    uint64_t d_empty[4];   // FP16 D stage consumed by the MMA
-    uint64_t i_full[4];    // INT8 staging tile landed
-    uint64_t i_empty[4];   // INT8 staging tile converted
+    uint64_t d_full[kMaxStages];    // FP16 D stage ready for the MMA
+    uint64_t d_empty[kMaxStages];   // FP16 D stage consumed by the MMA
+    uint64_t i_full[kMaxStages];    // INT8 staging tile landed
+    uint64_t i_empty[kMaxStages];   // INT8 staging tile converted
     uint64_t t_full[kSlots];
     uint64_t t_empty[kSlots];
     uint64_t mma_done;
@@ -63,13 +65,17 @@ template <int NMT, bool INT8>
 struct Cfg {
     static constexpr int kStages = INT8 ? (NMT == 4 ? 2 : 3) : (NMT == 4 ? 3 : 4);
     static constexpr int kI8Stages = INT8 ? (NMT == 4 ? 2 : 4) : 0;
-    static constexpr int kConvWarps = INT8 ? 4 : 0;
+    static constexpr int kConvWarps = INT8 ? (NMT == 4 ? 2 : 4) : 0;
+    static constexpr bool kDoubleBuffer = NMT < 4;
     static constexpr int kFirstEpiWarp = 2 + kConvWarps;
     static constexpr int kThreads = 32 * (kFirstEpiWarp + 4 * NMT);
     static constexpr int kQBytes = NMT * kTileBytes;
     static constexpr int kDBytes = kStages * kTileBytes;
     static constexpr int kIBytes = kI8Stages * kI8TileBytes;
     static constexpr int kSmem = 1024 + kQBytes + kDBytes + kIBytes + (int)sizeof(SharedCtl);
+    static_assert(kStages >= 1 && kStages <= kMaxStages, "barrier arrays hold kMaxStages stages");
+    static_assert(kI8Stages <= kMaxStages, "barrier arrays hold kMaxStages stages");
+    static_assert(kSmem <= 232448, "exceeds the 227 KB shared-memory limit per CTA");
 };
 
 __device__ __forceinline__ int lower_bound_cu(const int32_t *cu, int n, int64_t key) {
@@ -82,50 +88,88 @@ __device__ __forceinline__ int lower_bound_cu(const int32_t *cu, int n, int64_t 
     return lo;
 }
 
-// Running (max, lowest argmax) update with 32 candidate columns c0 + k.
-// A balanced tree: at every node the right (higher-index) candidate wins
-// only when strictly greater, so equal values keep the lowest index.
-__device__ __forceinline__ void fold_argmax32(const float (&v)[32], int c0, float &m, int &a) {
-    float x[16];
-    int ix[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-        const bool p = v[2 * k + 1] > v[2 * k];
-        x[k] = p ? v[2 * k + 1] : v[2 * k];
-        ix[k] = 2 * k + (p ? 1 : 0);
-    }
-#pragma unroll
-    for (int w = 8; w >= 1; w >>= 1) {
-#pragma unroll
-        for (int k = 0; k < w; ++k) {
-            const bool p = x[2 * k + 1] > x[2 * k];
-            x[k] = p ? x[2 * k + 1] : x[2 * k];
-            ix[k] = p ? ix[2 * k + 1] : ix[2 * k];
-        }
-    }
-    if (x[0] > m) {   // later columns win only when strictly greater
-        m = x[0];
-        a = c0 + ix[0];
-    }
+// Column k of a 32-column chunk of the accumulator; with MASKED, columns
+// outside [lo, hi) read as -inf so they can never be selected (the masking
+// of §4.1.1, applied before the reduction).
+template <bool MASKED>
+__device__ __forceinline__ float col(const uint32_t (&r)[32], int k, int lo, int hi) {
+    const float x = __uint_as_float(r[k]);
+    if (MASKED) return (k >= lo && k < hi) ? x : -INFINITY;
+    return x;
 }
 
-__device__ __forceinline__ float max32(const float (&v)[32]) {
+// Maximum of a chunk with 3-input max instructions (16 per 32 columns).
+template <bool MASKED>
+__device__ __forceinline__ float chunk_max(const uint32_t (&r)[32], int lo, int hi) {
     float y[11];
 #pragma unroll
-    for (int k = 0; k < 10; ++k) y[k] = fmax3(v[3 * k], v[3 * k + 1], v[3 * k + 2]);
-    y[10] = fmaxf(v[30], v[31]);
+    for (int k = 0; k < 10; ++k)
+        y[k] = fmax3(col<MASKED>(r, 3 * k, lo, hi), col<MASKED>(r, 3 * k + 1, lo, hi),
+                     col<MASKED>(r, 3 * k + 2, lo, hi));
+    y[10] = fmaxf(col<MASKED>(r, 30, lo, hi), col<MASKED>(r, 31, lo, hi));
     const float z0 = fmax3(y[0], y[1], y[2]);
     const float z1 = fmax3(y[3], y[4], y[5]);
     const float z2 = fmax3(y[6], y[7], y[8]);
-    const float z3 = fmaxf(y[9], y[10]);
-    return fmaxf(fmax3(z0, z1, z2), z3);
+    return fmax3(fmax3(z0, z1, z2), y[9], y[10]);
 }
 
-// Columns outside [lo, hi) of the chunk become -inf (never selected).
-__device__ __forceinline__ void mask_outside(float (&v)[32], int lo, int hi) {
+// Lowest column k with value == cm, where cm is the chunk's maximum.
+//
+// Each column contributes the indicator [value < cm] as an exact 0.0 / 1.0
+// computed on the FMA pipe (the ALU pipe that compares and selects run on
+// issues at half rate): with S = 2^100 and C = cm * S (exact),
+// fma.sat(value, -S, C) = sat(S * (cm - value)) is 0 when value == cm and 1
+// otherwise, because a nonzero cm - value is at least one ulp of cm, >= 2^-100
+// when |cm| >= 2^-77, and C stays finite when |cm| < 2^27 (`fast`).  Outside
+// that range two saturating multiplies of (cm - value) by 2^127 and 2^23 reach
+// 1 for every nonzero finite difference.  The indicators are packed into a
+// bit mask 8 at a time (sums of distinct powers of two below 2^8 are exact),
+// and the first clear bit is the lowest index attaining the maximum.
+template <bool MASKED>
+__device__ __forceinline__ int chunk_first_equal(const uint32_t (&r)[32], int lo, int hi, float cm,
+                                                 bool fast) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (fast) {
+        const float S = 0x1p100f;
+        const float C = cm * S;
 #pragma unroll
-    for (int k = 0; k < 32; ++k)
-        if (k < lo || k >= hi) v[k] = -INFINITY;
+        for (int k = 0; k < 32; ++k)
+            acc[k >> 3] = fmaf(fma_sat(col<MASKED>(r, k, lo, hi), -S, C), static_cast<float>(1u << (k & 7)),
+                               acc[k >> 3]);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            const float t = cm - col<MASKED>(r, k, lo, hi);
+            acc[k >> 3] = fmaf(mul_sat(mul_sat(t, 0x1p127f), 0x1p23f), static_cast<float>(1u << (k & 7)),
+                               acc[k >> 3]);
+        }
+    }
+    const uint32_t mask = static_cast<uint32_t>(acc[0]) | (static_cast<uint32_t>(acc[1]) << 8) |
+                          (static_cast<uint32_t>(acc[2]) << 16) | (static_cast<uint32_t>(acc[3]) << 24);
+    return __ffs(~mask) - 1;
+}
+
+// Fold columns [lo, hi) of a chunk starting at global column c0 into the
+// running row maximum m (and, with ARGMAX, its lowest index a).  Later
+// chunks replace the running winner only when strictly greater, so ties keep
+// the lowest column.  Must be called by the whole warp.
+template <bool ARGMAX, bool MASKED>
+__device__ __forceinline__ void fold_chunk(const uint32_t (&r)[32], int c0, int lo, int hi, float &m, int &a) {
+    const float cm = chunk_max<MASKED>(r, lo, hi);
+    if (!ARGMAX) {
+        m = fmaxf(m, cm);
+        return;
+    }
+    const bool up = cm > m;
+    if (__any_sync(0xffffffffu, up)) {
+        const float acm = fabsf(cm);
+        const bool fast = __all_sync(0xffffffffu, !up || (acm >= 0x1p-77f && acm < 0x1p27f));
+        const int k = chunk_first_equal<MASKED>(r, lo, hi, cm, fast);
+        if (up) {
+            m = cm;
+            a = c0 + k;
+        }
+    }
 }
 
 // int8 x4 -> fp16 x4 exactly: (x ^ 0x80) in the low byte of 1024.0 gives
@@ -165,11 +209,11 @@ maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
 
     if (threadIdx.x == 0) {
         mbar_init(&ctl->q_full, 1);
-        for (int s = 0; s < 4; ++s) {
-            mbar_init(&ctl->d_full[s], INT8 ? 128 : 1);
+        for (int s = 0; s < kMaxStages; ++s) {
+            mbar_init(&ctl->d_full[s], INT8 ? 32 * C::kConvWarps : 1);
             mbar_init(&ctl->d_empty[s], 1);
             mbar_init(&ctl->i_full[s], 1);
-            mbar_init(&ctl->i_empty[s], INT8 ? 128 : 1);
+            mbar_init(&ctl->i_empty[s], INT8 ? 32 * C::kConvWarps : 1);
         }
         for (int s = 0; s < kSlots; ++s) {
             mbar_init(&ctl->t_full[s], 1);
@@ -247,12 +291,16 @@ maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         if (lane == 0 && run_pipeline) {
             bool ok = mbar_wait(&ctl->q_full, 0, abort_flag, p.status, kStatusTimeoutMma);
             tc_fence_after();
-            const uint32_t q_base = smem_u32(sQ);
+            // Descriptors advance by adding (byte offset >> 4) to the start
+            // address field; every operand lies below 256 KB of shared memory,
+            // so the 14-bit field never carries.
+            const uint64_t a_desc0 = desc_sw128_kmajor(smem_u32(sQ));
+            const uint64_t b_desc0 = desc_sw128_kmajor(smem_u32(sD));
             for (int j = 0; ok && j < n_tiles; ++j) {
                 const int s = j % C::kStages;
                 if (!mbar_wait(&ctl->d_full[s], (j / C::kStages) & 1, abort_flag, p.status, kStatusTimeoutMma)) break;
                 tc_fence_after();
-                const uint32_t d_base = smem_u32(sD + s * kTileBytes);
+                const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((s * kTileBytes) >> 4);
                 for (int mt = 0; mt < n_mt; ++mt) {
                     const int slot = mt + NMT * (j % (kSlots / NMT));
                     const uint32_t use = j / (kSlots / NMT);
@@ -261,13 +309,12 @@ maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_base = q_base + mt * kTileBytes;
+                    const uint64_t a_desc = a_desc0 + static_cast<uint64_t>((mt * kTileBytes) >> 4);
                     const uint32_t d_tmem = tmem_base + slot * kSlotCols;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t koff = (kk >> 2) * kKBlockBytes + (kk & 3) * 32;
-                        mma_f16_ss(d_tmem, desc_sw128_kmajor(a_base + koff),
-                                   desc_sw128_kmajor(d_base + koff), p.idesc, kk > 0 ? 1u : 0u);
+                        const uint64_t koff = static_cast<uint64_t>(((kk >> 2) * kKBlockBytes + (kk & 3) * 32) >> 4);
+                        mma_f16_ss(d_tmem, a_desc + koff, b_desc + koff, p.idesc, kk > 0 ? 1u : 0u);
                     }
                     mma_commit(&ctl->t_full[slot]);
                 }
@@ -280,13 +327,15 @@ maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         __syncwarp();
     } else if (warp < C::kFirstEpiWarp) {
         // ------------------------------------------------ INT8 -> FP16 widening
-        const int t = threadIdx.x - 64;  // row of the tile, 0..127
+        const int t0 = threadIdx.x - 64;  // first row of the tile this thread widens
         if constexpr (INT8) if (run_pipeline) {
             for (int j = 0; j < n_tiles; ++j) {
                 const int si = j % C::kI8Stages;
                 const int sd = j % C::kStages;
                 if (!mbar_wait(&ctl->i_full[si], (j / C::kI8Stages) & 1, abort_flag, p.status, kStatusTimeoutProducer)) break;
                 if (!mbar_wait(&ctl->d_empty[sd], ((j / C::kStages) & 1) ^ 1, abort_flag, p.status, kStatusTimeoutProducer)) break;
+#pragma unroll 1
+                for (int t = t0; t < 128; t += 32 * C::kConvWarps) {
                 const uint8_t *src = sI + si * kI8TileBytes + t * 128;
                 uint8_t *dst = sD + sd * kTileBytes + t * 128;
 #pragma unroll
@@ -300,6 +349,7 @@ maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                     const int c16 = 2 * (c & 3);
                     *reinterpret_cast<uint4 *>(kb + ((c16 ^ (t & 7)) << 4)) = make_uint4(e0.x, e0.y, e1.x, e1.y);
                     *reinterpret_cast<uint4 *>(kb + (((c16 + 1) ^ (t & 7)) << 4)) = make_uint4(e2.x, e2.y, e3.x, e3.y);
+                }
                 }
                 fence_proxy_async_smem();   // generic-proxy writes -> visible to the tensor core
                 mbar_arrive(&ctl->i_empty[si]);
@@ -321,13 +371,27 @@ maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             const bool active = row_valid && i < qlen;
             const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
 
+            // Upcoming document boundaries: lane l holds cu[cu_base + l]; one
+            // coalesced load serves 32 documents, read back by shuffles.
+            int cu_base = b_begin + 1;
+            int cu_val = (cu_base + lane <= b_end) ? p.cu_seqlens[cu_base + lane] : INT32_MAX;
+            auto boundary = [&](int idx) -> int {  // cu[idx], idx warp-uniform in (b_begin, b_end]
+                if (idx >= cu_base + 32) {
+                    cu_base = idx;
+                    cu_val = (cu_base + lane <= b_end) ? p.cu_seqlens[cu_base + lane] : INT32_MAX;
+                }
+                return __shfl_sync(0xffffffffu, cu_val, idx - cu_base);
+            };
+
             float m = -INFINITY;
             int a = -1;
             int b = b_begin;
             int doc_lo = t_begin;
-            int doc_hi = (b < b_end) ? p.cu_seqlens[b + 1] : INT32_MAX;
+            int doc_hi = (b < b_end) ? boundary(b + 1) : INT32_MAX;
             bool aborted = false;
 
+            // End of document b for this warp's rows: argmax row, then the
+            // sum of row maxima over the query's tokens (fixed shuffle tree).
             auto finalize = [&]() {
                 if (ARGMAX && row_valid)
                     p.argmax[(static_cast<int64_t>(q) * p.n_docs + b) * p.lq_max + i] =
@@ -364,9 +428,27 @@ maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                 a = -1;
                 ++b;
                 doc_lo = doc_hi;
-                doc_hi = (b < b_end) ? p.cu_seqlens[b + 1] : INT32_MAX;
+                doc_hi = (b < b_end) ? boundary(b + 1) : INT32_MAX;
             };
 
+            // Columns c0 .. c0+31 of the current tile: split at document ends.
+            auto process = [&](const uint32_t (&r)[32], int c0) {
+                const int cend = min(c0 + 32, t_end);
+                int c = c0;
+                while (c < cend) {
+                    if (doc_hi <= c) {
+                        finalize();
+                        continue;
+                    }
+                    const int seg_end = min(doc_hi, cend);
+                    if (c == c0 && seg_end == c0 + 32) fold_chunk<ARGMAX, false>(r, c0, 0, 32, m, a);
+                    else fold_chunk<ARGMAX, true>(r, c0, c - c0, seg_end - c0, m, a);
+                    c = seg_end;
+                }
+            };
+
+            uint32_t ra[32];
+            [[maybe_unused]] uint32_t rb[32];
             for (int j = 0; j < n_tiles; ++j) {
                 const int slot = mt + NMT * (j % (kSlots / NMT));
                 const uint32_t use = j / (kSlots / NMT);
@@ -375,36 +457,52 @@ maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                     break;
                 }
                 tc_fence_after();
-                const int tile0 = t_begin + j * kBlockN;
-#pragma unroll
-                for (int kc = 0; kc < 4; ++kc) {
-                    float v[32];
+                if (!warp_rows) {
+                    tc_fence_before();
                     __syncwarp();
-                    if (warp_rows) tmem_ld32(tmem_base + lane_base + slot * kSlotCols + kc * 32, v);
-                    if (kc == 3) {
-                        tc_fence_before();
+                    if (lane == 0) mbar_arrive(&ctl->t_empty[slot]);
+                    continue;
+                }
+                const uint32_t tb = tmem_base + lane_base + slot * kSlotCols;
+                const int tile0 = t_begin + j * kBlockN;
+                if constexpr (C::kDoubleBuffer) {
+                    // four 32-column chunks, the next one loading while one is folded
+                    __syncwarp();
+                    tmem_ld32_async(tb, ra);
+                    tmem_wait_ld(ra);
+#pragma unroll 1
+                    for (int h = 0; h < 2; ++h) {
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(&ctl->t_empty[slot]);
-                    }
-                    if (!warp_rows) continue;
-                    const int c0 = tile0 + kc * 32;
-                    const int cend = min(c0 + 32, t_end);
-                    int c = c0;
-                    while (c < cend) {
-                        while (doc_hi <= c) finalize();
-                        const int seg_end = min(doc_hi, cend);
-                        if (c == c0 && seg_end == c0 + 32) {
-                            if (ARGMAX) fold_argmax32(v, c0, m, a);
-                            else m = fmaxf(m, max32(v));
+                        tmem_ld32_async(tb + 64 * h + 32, rb);
+                        process(ra, tile0 + 64 * h);
+                        __syncwarp();
+                        tmem_wait_ld(rb);
+                        if (h == 0) {
+                            tmem_ld32_async(tb + 64, ra);
                         } else {
-                            float w[32];
-#pragma unroll
-                            for (int k = 0; k < 32; ++k) w[k] = v[k];
-                            mask_outside(w, c - c0, seg_end - c0);
-                            if (ARGMAX) fold_argmax32(w, c0, m, a);
-                            else m = fmaxf(m, max32(w));
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&ctl->t_empty[slot]);
                         }
-                        c = seg_end;
+                        process(rb, tile0 + 64 * h + 32);
+                        if (h == 0) {
+                            __syncwarp();
+                            tmem_wait_ld(ra);
+                        }
+                    }
+                } else {
+                    // registers are scarce at 4 M-tiles: one chunk at a time
+#pragma unroll 1
+                    for (int kc = 0; kc < 4; ++kc) {
+                        __syncwarp();
+                        tmem_ld32_async(tb + 32 * kc, ra);
+                        tmem_wait_ld(ra);
+                        if (kc == 3) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&ctl->t_empty[slot]);
+                        }
+                        process(ra, tile0 + 32 * kc);
                     }
                 }
             }
