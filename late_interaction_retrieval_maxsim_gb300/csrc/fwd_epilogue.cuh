@@ -1,0 +1,395 @@
+// fwd_epilogue.cuh -- the epilogue shared by the fused MaxSim forward
+// kernels: fold TMEM accumulator tiles into running row maxima (and their
+// lowest argmax), split at document boundaries, and reduce over query tokens
+// at each document's end.
+//
+// "FLASH-MAXSIM: IO-Aware Fused Kernels for Late-Interaction Retrieval"
+// (arXiv 2605.29517) §4.1.1 (online-max recurrence, masking to -inf before
+// the reduction), §4.1 (query-chunk decomposition of the sum), §4.3.2
+// (documents packed with cu_seqlens).
+#pragma once
+
+#include "internal.cuh"
+#include "sm103.cuh"
+
+#include <cuda_fp16.h>
+
+namespace maxsim {
+namespace {
+
+using namespace ptx;
+
+constexpr int kBlockN = 128;    // document tokens per tile (MMA N)
+constexpr int kSlotCols = 128;  // TMEM columns per accumulator slot
+
+__device__ __forceinline__ int lower_bound_cu(const int32_t *cu, int n, int64_t key) {
+    // first index in [0, n] with cu[index] >= key (cu[n] is the token total)
+    int lo = 0, hi = n;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (static_cast<int64_t>(cu[mid]) >= key) hi = mid; else lo = mid + 1;
+    }
+    return lo;
+}
+
+// Column k of a 32-column chunk of the accumulator; with MASKED, columns
+// outside [lo, hi) read as -inf so they can never be selected (the masking
+// of §4.1.1, applied before the reduction).
+template <bool MASKED>
+__device__ __forceinline__ float col(const uint32_t (&r)[32], int k, int lo, int hi) {
+    const float x = __uint_as_float(r[k]);
+    if (MASKED) return (k >= lo && k < hi) ? x : -INFINITY;
+    return x;
+}
+
+// Maximum of a chunk with 3-input max instructions (16 per 32 columns).
+template <bool MASKED>
+__device__ __forceinline__ float chunk_max(const uint32_t (&r)[32], int lo, int hi) {
+    float y[11];
+#pragma unroll
+    for (int k = 0; k < 10; ++k)
+        y[k] = fmax3(col<MASKED>(r, 3 * k, lo, hi), col<MASKED>(r, 3 * k + 1, lo, hi),
+                     col<MASKED>(r, 3 * k + 2, lo, hi));
+    y[10] = fmaxf(col<MASKED>(r, 30, lo, hi), col<MASKED>(r, 31, lo, hi));
+    const float z0 = fmax3(y[0], y[1], y[2]);
+    const float z1 = fmax3(y[3], y[4], y[5]);
+    const float z2 = fmax3(y[6], y[7], y[8]);
+    return fmax3(fmax3(z0, z1, z2), y[9], y[10]);
+}
+
+// True when the one-instruction indicator below is exact for maximum cm.
+__device__ __forceinline__ bool fast_indicator_ok(float cm) {
+    const float x = fabsf(cm);
+    return x >= 0x1p-77f && x < 0x1p27f;
+}
+
+// Bit k set when column k holds a value below cm, clear when it equals cm
+// (columns above cm, which only occur outside a segment, come out clear and
+// must be masked by the caller).
+//
+// Each column's indicator is an exact 0.0 / 1.0 computed on the FMA pipe
+// (the ALU pipe that compares and selects use issues at half rate): with
+// S = 2^100 and C = cm * S (exact), fma.sat(value, -S, C) = sat(S * (cm -
+// value)) is 0 when value == cm and 1 when value < cm, because a nonzero
+// cm - value is at least one ulp of cm, >= 2^-100 when |cm| >= 2^-77, and C
+// stays finite when |cm| < 2^27 (`fast`).  Otherwise two saturating
+// multiplies of (cm - value) by 2^127 and 2^23 reach 1 for every nonzero
+// finite difference.  Indicators are packed into the mask 8 at a time (sums
+// of distinct powers of two below 2^16 are exact in FP32).
+__device__ __forceinline__ uint32_t below_mask32(const uint32_t (&r)[32], float cm, bool fast) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (fast) {
+        const float S = 0x1p100f;
+        const float C = cm * S;
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+            acc[k >> 3] = fmaf(fma_sat(__uint_as_float(r[k]), -S, C), static_cast<float>(1u << (k & 7)),
+                               acc[k >> 3]);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            const float t = cm - __uint_as_float(r[k]);
+            acc[k >> 3] = fmaf(mul_sat(mul_sat(t, 0x1p127f), 0x1p23f), static_cast<float>(1u << (k & 7)),
+                               acc[k >> 3]);
+        }
+    }
+    const float lo = fmaf(acc[1], 256.f, acc[0]);
+    const float hi = fmaf(acc[3], 256.f, acc[2]);
+    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+// Bits lo .. hi-1 set (0 <= lo < hi <= 32).
+__device__ __forceinline__ uint32_t bit_range(int lo, int hi) {
+    const uint32_t upto_hi = hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u);
+    return upto_hi & ~((1u << lo) - 1u);
+}
+
+// Fold columns [lo, hi) of a chunk starting at global column c0 into the
+// running row maximum m (and, with ARGMAX, its lowest index a).  Later
+// chunks replace the running winner only when strictly greater, so ties keep
+// the lowest column.  Must be called by the whole warp.
+template <bool ARGMAX, bool MASKED>
+__device__ __forceinline__ void fold_chunk(const uint32_t (&r)[32], int c0, int lo, int hi, float &m, int &a) {
+    const float cm = chunk_max<MASKED>(r, lo, hi);
+    if (!ARGMAX) {
+        m = fmaxf(m, cm);
+        return;
+    }
+    const bool up = cm > m;
+    if (__any_sync(0xffffffffu, up)) {
+        const bool fast = __all_sync(0xffffffffu, !up || fast_indicator_ok(cm));
+        uint32_t mask = below_mask32(r, cm, fast);
+        if (MASKED) mask |= ~bit_range(lo, hi);
+        if (up) {
+            m = cm;
+            a = c0 + __ffs(~mask) - 1;
+        }
+    }
+}
+
+template <int B>
+__device__ __forceinline__ float max8(const uint32_t (&r)[32]) {
+    auto f = [&](int k) { return __uint_as_float(r[B + k]); };
+    return fmax3(fmax3(f(0), f(1), f(2)), fmax3(f(3), f(4), f(5)), fmaxf(f(6), f(7)));
+}
+
+// Columns B .. B+7 split at o (0 <= o < 8, warp-uniform): maxima of
+// [B, B+o) and [B+o, B+8), -inf for an empty side.
+template <int B>
+__device__ __forceinline__ void split8(const uint32_t (&r)[32], int o, float &below, float &above) {
+    float x[8], y[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float v = __uint_as_float(r[B + k]);
+        x[k] = k < o ? v : -INFINITY;
+        y[k] = k < o ? -INFINITY : v;
+    }
+    below = fmax3(fmax3(x[0], x[1], x[2]), fmax3(x[3], x[4], x[5]), fmaxf(x[6], x[7]));
+    above = fmax3(fmax3(y[0], y[1], y[2]), fmax3(y[3], y[4], y[5]), fmaxf(y[6], y[7]));
+}
+
+// Maxima of columns [0, p) and [p, 32) for a document boundary at p
+// (1 <= p <= 31): eight-column group maxima, with only the group holding the
+// boundary masked column by column.
+__device__ __forceinline__ void split_max32(const uint32_t (&r)[32], int p, float &left, float &right) {
+    const float g0 = max8<0>(r), g1 = max8<8>(r), g2 = max8<16>(r), g3 = max8<24>(r);
+    const int o = p & 7;
+    float lo, hi;
+    switch (p >> 3) {
+        case 0:
+            split8<0>(r, o, lo, hi);
+            left = lo;
+            right = fmax3(hi, g1, fmaxf(g2, g3));
+            break;
+        case 1:
+            split8<8>(r, o, lo, hi);
+            left = fmaxf(g0, lo);
+            right = fmax3(hi, g2, g3);
+            break;
+        case 2:
+            split8<16>(r, o, lo, hi);
+            left = fmax3(g0, g1, lo);
+            right = fmaxf(hi, g3);
+            break;
+        default:
+            split8<24>(r, o, lo, hi);
+            left = fmax3(g0, g1, fmaxf(g2, lo));
+            right = hi;
+            break;
+    }
+}
+
+// A chunk in which the current document ends at column p (1 <= p <= 31) and
+// the next one covers the rest: [0, p) is folded into (m, a); the next
+// document's running state starts as (m_next, a_next) from [p, 32).
+template <bool ARGMAX>
+__device__ __forceinline__ void fold_split(const uint32_t (&r)[32], int c0, int p, float &m, int &a,
+                                           float &m_next, int &a_next) {
+    float left, right;
+    split_max32(r, p, left, right);
+    if (!ARGMAX) {
+        m = fmaxf(m, left);
+        m_next = right;
+        return;
+    }
+    const bool up = left > m;
+    const uint32_t low = (1u << p) - 1u;
+    const bool fast = __all_sync(0xffffffffu, fast_indicator_ok(right) && (!up || fast_indicator_ok(left)));
+    m_next = right;
+    a_next = c0 + __ffs(~(below_mask32(r, right, fast) | low)) - 1;
+    if (__any_sync(0xffffffffu, up)) {
+        const uint32_t mask = below_mask32(r, left, fast) | ~low;
+        if (up) {
+            m = left;
+            a = c0 + __ffs(~mask) - 1;
+        }
+    }
+}
+
+// One epilogue warp owns 32 consecutive padded query rows (rho_warp ..
+// rho_warp+31) of an accumulator tile that lives in TMEM lane quarter qd.
+// For every document tile j it waits t_full[slot_of(j).x] (phase
+// slot_of(j).y), reads the 128 columns 32 at a time, hands the slot back
+// with release(slot) once the last chunk is in registers, and folds the
+// chunks into the running maxima; at each document end it writes the argmax
+// row and the (partial) score.  DB double-buffers the TMEM reads.
+template <bool ARGMAX, bool INT8, bool DB, typename SlotOf, typename Release>
+__device__ __forceinline__ void epilogue_warp(const FwdParams &p, int rho_warp, int64_t rows_total,
+                                              uint32_t tmem_base, int qd, int b_begin, int b_end,
+                                              int t_begin, int t_end, int n_tiles, uint64_t *t_full,
+                                              SlotOf slot_of, Release release,
+                                              volatile int32_t *abort_flag, bool cluster_scope) {
+    const int lane = threadIdx.x & 31;
+    const bool warp_rows = rho_warp < rows_total;
+    const int rho = rho_warp + lane;
+    const int q = rho / p.lq_pad;
+    const int i = rho - q * p.lq_pad;
+    const bool row_valid = q < p.n_q && i < p.lq_max;
+    const int qlen = (q < p.n_q) ? p.q_lens[q] : 0;
+    const bool active = row_valid && i < qlen;
+    const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
+
+    // Upcoming document boundaries: lane l holds cu[cu_base + l]; one
+    // coalesced load serves 32 documents, read back by shuffles.
+    int cu_base = b_begin + 1;
+    int cu_val = (cu_base + lane <= b_end) ? p.cu_seqlens[cu_base + lane] : INT32_MAX;
+    auto boundary = [&](int idx) -> int {  // cu[idx], idx warp-uniform in (b_begin, b_end]
+        if (idx >= cu_base + 32) {
+            cu_base = idx;
+            cu_val = (cu_base + lane <= b_end) ? p.cu_seqlens[cu_base + lane] : INT32_MAX;
+        }
+        return __shfl_sync(0xffffffffu, cu_val, idx - cu_base);
+    };
+
+    float m = -INFINITY;
+    int a = -1;
+    int b = b_begin;
+    int doc_lo = t_begin;
+    int doc_hi = (b < b_end) ? boundary(b + 1) : INT32_MAX;
+    bool aborted = false;
+
+    // End of document b for this warp's rows: argmax row, then the
+    // sum of row maxima over the query's tokens (fixed shuffle tree).
+    auto finalize = [&]() {
+        if (ARGMAX && row_valid)
+            p.argmax[(static_cast<int64_t>(q) * p.n_docs + b) * p.lq_max + i] =
+                (active && a >= 0) ? a - doc_lo : -1;
+        if (INT8) {
+            const bool empty_doc = doc_hi == doc_lo;
+            long long c = (active && !empty_doc) ? static_cast<long long>(m) : 0ll;
+            if (p.lq_pad <= 32) {
+                for (int off = 1; off < p.lq_pad; off <<= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
+                if (i == 0 && q < p.n_q) {
+                    const bool neg_inf = empty_doc && qlen > 0;
+                    const int64_t idx = static_cast<int64_t>(q) * p.n_docs + b;
+                    if (p.raw_scores) p.raw_scores[idx] = neg_inf ? INT64_MIN : c;
+                    p.scores[idx] = neg_inf ? -INFINITY
+                                            : static_cast<float>(static_cast<double>(c) * p.int8_scale);
+                }
+            } else {
+                for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
+                if (lane == 0 && q < p.n_q)
+                    p.ipartials[(static_cast<int64_t>(i >> 5) * p.n_q + q) * p.n_docs + b] = c;
+            }
+        } else {
+            float c = active ? m : 0.0f;
+            if (p.lq_pad == 32) {
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
+                if (lane == 0 && q < p.n_q) p.scores[static_cast<int64_t>(q) * p.n_docs + b] = c;
+            } else if (p.lq_pad < 32) {
+                for (int off = 1; off < p.lq_pad; off <<= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
+                if (i == 0 && q < p.n_q) p.scores[static_cast<int64_t>(q) * p.n_docs + b] = c;
+            } else {
+                for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
+                if (lane == 0 && q < p.n_q)
+                    p.partials[(static_cast<int64_t>(i >> 5) * p.n_q + q) * p.n_docs + b] = c;
+            }
+        }
+        m = -INFINITY;
+        a = -1;
+        ++b;
+        doc_lo = doc_hi;
+        doc_hi = (b < b_end) ? boundary(b + 1) : INT32_MAX;
+    };
+
+    // Columns c0 .. c0+31 of the current tile: split at document ends.
+    auto process = [&](const uint32_t (&r)[32], int c0) {
+        if (c0 >= t_end) return;                 // past the last document of this CTA
+        while (doc_hi <= c0) finalize();         // documents ending at the chunk start (or empty)
+        if (doc_hi >= c0 + 32) {                 // the whole chunk lies in the current document
+            fold_chunk<ARGMAX, false>(r, c0, 0, 32, m, a);
+            return;
+        }
+        if (c0 + 32 <= t_end && b + 1 < b_end && boundary(b + 2) >= c0 + 32) {
+            // exactly one document boundary inside the chunk
+            float m_next;
+            int a_next = -1;
+            fold_split<ARGMAX>(r, c0, doc_hi - c0, m, a, m_next, a_next);
+            finalize();
+            m = m_next;
+            a = a_next;
+            return;
+        }
+        // several boundaries, or the end of this CTA's documents
+        const int cend = min(c0 + 32, t_end);
+        int c = c0;
+        while (c < cend) {
+            if (doc_hi <= c) {
+                finalize();
+                continue;
+            }
+            const int seg_end = min(doc_hi, cend);
+            if (c == c0 && seg_end == c0 + 32) fold_chunk<ARGMAX, false>(r, c0, 0, 32, m, a);
+            else fold_chunk<ARGMAX, true>(r, c0, c - c0, seg_end - c0, m, a);
+            c = seg_end;
+        }
+    };
+
+    uint32_t ra[32];
+    [[maybe_unused]] uint32_t rb[32];
+    for (int j = 0; j < n_tiles; ++j) {
+        const int2 su = slot_of(j);
+        const int slot = su.x;
+        const uint32_t use = static_cast<uint32_t>(su.y);
+        if (!(cluster_scope ? mbar_wait_cluster(&t_full[slot], use & 1, abort_flag, p.status, kStatusTimeoutEpilogue)
+                            : mbar_wait(&t_full[slot], use & 1, abort_flag, p.status, kStatusTimeoutEpilogue))) {
+            aborted = true;
+            break;
+        }
+        tc_fence_after();
+        if (!warp_rows) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) release(slot);
+            continue;
+        }
+        const uint32_t tb = tmem_base + lane_base + slot * kSlotCols;
+        const int tile0 = t_begin + j * kBlockN;
+        if constexpr (DB) {
+            // four 32-column chunks, the next one loading while one is folded
+            __syncwarp();
+            tmem_ld32_async(tb, ra);
+            tmem_wait_ld(ra);
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                __syncwarp();
+                tmem_ld32_async(tb + 64 * h + 32, rb);
+                process(ra, tile0 + 64 * h);
+                __syncwarp();
+                tmem_wait_ld(rb);
+                if (h == 0) {
+                    tmem_ld32_async(tb + 64, ra);
+                } else {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) release(slot);
+                }
+                process(rb, tile0 + 64 * h + 32);
+                if (h == 0) {
+                    __syncwarp();
+                    tmem_wait_ld(ra);
+                }
+            }
+        } else {
+            // registers are scarce at 4 M-tiles: one chunk at a time
+#pragma unroll 1
+            for (int kc = 0; kc < 4; ++kc) {
+                __syncwarp();
+                tmem_ld32_async(tb + 32 * kc, ra);
+                tmem_wait_ld(ra);
+                if (kc == 3) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) release(slot);
+                }
+                process(ra, tile0 + 32 * kc);
+            }
+        }
+    }
+    if (!aborted && warp_rows)
+        while (b < b_end) finalize();
+}
+
+}  // namespace
+}  // namespace maxsim

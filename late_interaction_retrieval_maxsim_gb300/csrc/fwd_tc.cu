@@ -28,6 +28,7 @@
 //    exact int32 dot product, and sums over query tokens run in int64.
 #include "internal.cuh"
 #include "sm103.cuh"
+#include "fwd_epilogue.cuh"
 
 #include <cuda_fp16.h>
 
@@ -36,12 +37,10 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kBlockN = 128;                   // document tokens per tile (MMA N)
 constexpr int kKBlockBytes = 128 * 128;        // 128 rows x 64 16-bit elements, 128B-swizzled
 constexpr int kTileBytes = 2 * kKBlockBytes;   // 128 rows x 128 16-bit elements
 constexpr int kI8TileBytes = 128 * 128;        // 128 rows x 128 int8
 constexpr int kSlots = 4;                      // TMEM accumulator slots
-constexpr int kSlotCols = 128;
 constexpr int kTmemCols = kSlots * kSlotCols;  // 512: the whole TMEM
 
 constexpr int kMaxStages = 4;
@@ -77,100 +76,6 @@ struct Cfg {
     static_assert(kI8Stages <= kMaxStages, "barrier arrays hold kMaxStages stages");
     static_assert(kSmem <= 232448, "exceeds the 227 KB shared-memory limit per CTA");
 };
-
-__device__ __forceinline__ int lower_bound_cu(const int32_t *cu, int n, int64_t key) {
-    // first index in [0, n] with cu[index] >= key (cu[n] is the token total)
-    int lo = 0, hi = n;
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (static_cast<int64_t>(cu[mid]) >= key) hi = mid; else lo = mid + 1;
-    }
-    return lo;
-}
-
-// Column k of a 32-column chunk of the accumulator; with MASKED, columns
-// outside [lo, hi) read as -inf so they can never be selected (the masking
-// of §4.1.1, applied before the reduction).
-template <bool MASKED>
-__device__ __forceinline__ float col(const uint32_t (&r)[32], int k, int lo, int hi) {
-    const float x = __uint_as_float(r[k]);
-    if (MASKED) return (k >= lo && k < hi) ? x : -INFINITY;
-    return x;
-}
-
-// Maximum of a chunk with 3-input max instructions (16 per 32 columns).
-template <bool MASKED>
-__device__ __forceinline__ float chunk_max(const uint32_t (&r)[32], int lo, int hi) {
-    float y[11];
-#pragma unroll
-    for (int k = 0; k < 10; ++k)
-        y[k] = fmax3(col<MASKED>(r, 3 * k, lo, hi), col<MASKED>(r, 3 * k + 1, lo, hi),
-                     col<MASKED>(r, 3 * k + 2, lo, hi));
-    y[10] = fmaxf(col<MASKED>(r, 30, lo, hi), col<MASKED>(r, 31, lo, hi));
-    const float z0 = fmax3(y[0], y[1], y[2]);
-    const float z1 = fmax3(y[3], y[4], y[5]);
-    const float z2 = fmax3(y[6], y[7], y[8]);
-    return fmax3(fmax3(z0, z1, z2), y[9], y[10]);
-}
-
-// Lowest column k with value == cm, where cm is the chunk's maximum.
-//
-// Each column contributes the indicator [value < cm] as an exact 0.0 / 1.0
-// computed on the FMA pipe (the ALU pipe that compares and selects run on
-// issues at half rate): with S = 2^100 and C = cm * S (exact),
-// fma.sat(value, -S, C) = sat(S * (cm - value)) is 0 when value == cm and 1
-// otherwise, because a nonzero cm - value is at least one ulp of cm, >= 2^-100
-// when |cm| >= 2^-77, and C stays finite when |cm| < 2^27 (`fast`).  Outside
-// that range two saturating multiplies of (cm - value) by 2^127 and 2^23 reach
-// 1 for every nonzero finite difference.  The indicators are packed into a
-// bit mask 8 at a time (sums of distinct powers of two below 2^8 are exact),
-// and the first clear bit is the lowest index attaining the maximum.
-template <bool MASKED>
-__device__ __forceinline__ int chunk_first_equal(const uint32_t (&r)[32], int lo, int hi, float cm,
-                                                 bool fast) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (fast) {
-        const float S = 0x1p100f;
-        const float C = cm * S;
-#pragma unroll
-        for (int k = 0; k < 32; ++k)
-            acc[k >> 3] = fmaf(fma_sat(col<MASKED>(r, k, lo, hi), -S, C), static_cast<float>(1u << (k & 7)),
-                               acc[k >> 3]);
-    } else {
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            const float t = cm - col<MASKED>(r, k, lo, hi);
-            acc[k >> 3] = fmaf(mul_sat(mul_sat(t, 0x1p127f), 0x1p23f), static_cast<float>(1u << (k & 7)),
-                               acc[k >> 3]);
-        }
-    }
-    const uint32_t mask = static_cast<uint32_t>(acc[0]) | (static_cast<uint32_t>(acc[1]) << 8) |
-                          (static_cast<uint32_t>(acc[2]) << 16) | (static_cast<uint32_t>(acc[3]) << 24);
-    return __ffs(~mask) - 1;
-}
-
-// Fold columns [lo, hi) of a chunk starting at global column c0 into the
-// running row maximum m (and, with ARGMAX, its lowest index a).  Later
-// chunks replace the running winner only when strictly greater, so ties keep
-// the lowest column.  Must be called by the whole warp.
-template <bool ARGMAX, bool MASKED>
-__device__ __forceinline__ void fold_chunk(const uint32_t (&r)[32], int c0, int lo, int hi, float &m, int &a) {
-    const float cm = chunk_max<MASKED>(r, lo, hi);
-    if (!ARGMAX) {
-        m = fmaxf(m, cm);
-        return;
-    }
-    const bool up = cm > m;
-    if (__any_sync(0xffffffffu, up)) {
-        const float acm = fabsf(cm);
-        const bool fast = __all_sync(0xffffffffu, !up || (acm >= 0x1p-77f && acm < 0x1p27f));
-        const int k = chunk_first_equal<MASKED>(r, lo, hi, cm, fast);
-        if (up) {
-            m = cm;
-            a = c0 + k;
-        }
-    }
-}
 
 // int8 x4 -> fp16 x4 exactly: (x ^ 0x80) in the low byte of 1024.0 gives
 // 1024 + x + 128; subtracting 1152 leaves x.
@@ -361,156 +266,15 @@ maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         const int mt = (warp - C::kFirstEpiWarp) >> 2;
         const int qd = warp & 3;  // TMEM lane quarter this warp may access
         if (mt < n_mt) {
-            const int rho_warp = row0 + mt * 128 + qd * 32;
-            const bool warp_rows = rho_warp < rows_total;
-            const int rho = rho_warp + lane;
-            const int q = rho / p.lq_pad;
-            const int i = rho - q * p.lq_pad;
-            const bool row_valid = q < p.n_q && i < p.lq_max;
-            const int qlen = (q < p.n_q) ? p.q_lens[q] : 0;
-            const bool active = row_valid && i < qlen;
-            const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
-
-            // Upcoming document boundaries: lane l holds cu[cu_base + l]; one
-            // coalesced load serves 32 documents, read back by shuffles.
-            int cu_base = b_begin + 1;
-            int cu_val = (cu_base + lane <= b_end) ? p.cu_seqlens[cu_base + lane] : INT32_MAX;
-            auto boundary = [&](int idx) -> int {  // cu[idx], idx warp-uniform in (b_begin, b_end]
-                if (idx >= cu_base + 32) {
-                    cu_base = idx;
-                    cu_val = (cu_base + lane <= b_end) ? p.cu_seqlens[cu_base + lane] : INT32_MAX;
-                }
-                return __shfl_sync(0xffffffffu, cu_val, idx - cu_base);
-            };
-
-            float m = -INFINITY;
-            int a = -1;
-            int b = b_begin;
-            int doc_lo = t_begin;
-            int doc_hi = (b < b_end) ? boundary(b + 1) : INT32_MAX;
-            bool aborted = false;
-
-            // End of document b for this warp's rows: argmax row, then the
-            // sum of row maxima over the query's tokens (fixed shuffle tree).
-            auto finalize = [&]() {
-                if (ARGMAX && row_valid)
-                    p.argmax[(static_cast<int64_t>(q) * p.n_docs + b) * p.lq_max + i] =
-                        (active && a >= 0) ? a - doc_lo : -1;
-                if (INT8) {
-                    const bool empty_doc = doc_hi == doc_lo;
-                    long long c = (active && !empty_doc) ? static_cast<long long>(m) : 0ll;
-                    if (p.lq_pad <= 32) {
-                        for (int off = 1; off < p.lq_pad; off <<= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
-                        if (i == 0 && q < p.n_q) {
-                            const bool neg_inf = empty_doc && qlen > 0;
-                            const int64_t idx = static_cast<int64_t>(q) * p.n_docs + b;
-                            if (p.raw_scores) p.raw_scores[idx] = neg_inf ? INT64_MIN : c;
-                            p.scores[idx] = neg_inf ? -INFINITY
-                                                    : static_cast<float>(static_cast<double>(c) * p.int8_scale);
-                        }
-                    } else {
-                        for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
-                        if (lane == 0 && q < p.n_q)
-                            p.ipartials[(static_cast<int64_t>(i >> 5) * p.n_q + q) * p.n_docs + b] = c;
-                    }
-                } else {
-                    float c = active ? m : 0.0f;
-                    if (p.lq_pad <= 32) {
-                        for (int off = 1; off < p.lq_pad; off <<= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
-                        if (i == 0 && q < p.n_q) p.scores[static_cast<int64_t>(q) * p.n_docs + b] = c;
-                    } else {
-                        for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
-                        if (lane == 0 && q < p.n_q)
-                            p.partials[(static_cast<int64_t>(i >> 5) * p.n_q + q) * p.n_docs + b] = c;
-                    }
-                }
-                m = -INFINITY;
-                a = -1;
-                ++b;
-                doc_lo = doc_hi;
-                doc_hi = (b < b_end) ? boundary(b + 1) : INT32_MAX;
-            };
-
-            // Columns c0 .. c0+31 of the current tile: split at document ends.
-            auto process = [&](const uint32_t (&r)[32], int c0) {
-                const int cend = min(c0 + 32, t_end);
-                int c = c0;
-                while (c < cend) {
-                    if (doc_hi <= c) {
-                        finalize();
-                        continue;
-                    }
-                    const int seg_end = min(doc_hi, cend);
-                    if (c == c0 && seg_end == c0 + 32) fold_chunk<ARGMAX, false>(r, c0, 0, 32, m, a);
-                    else fold_chunk<ARGMAX, true>(r, c0, c - c0, seg_end - c0, m, a);
-                    c = seg_end;
-                }
-            };
-
-            uint32_t ra[32];
-            [[maybe_unused]] uint32_t rb[32];
-            for (int j = 0; j < n_tiles; ++j) {
-                const int slot = mt + NMT * (j % (kSlots / NMT));
-                const uint32_t use = j / (kSlots / NMT);
-                if (!mbar_wait(&ctl->t_full[slot], use & 1, abort_flag, p.status, kStatusTimeoutEpilogue)) {
-                    aborted = true;
-                    break;
-                }
-                tc_fence_after();
-                if (!warp_rows) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&ctl->t_empty[slot]);
-                    continue;
-                }
-                const uint32_t tb = tmem_base + lane_base + slot * kSlotCols;
-                const int tile0 = t_begin + j * kBlockN;
-                if constexpr (C::kDoubleBuffer) {
-                    // four 32-column chunks, the next one loading while one is folded
-                    __syncwarp();
-                    tmem_ld32_async(tb, ra);
-                    tmem_wait_ld(ra);
-#pragma unroll 1
-                    for (int h = 0; h < 2; ++h) {
-                        __syncwarp();
-                        tmem_ld32_async(tb + 64 * h + 32, rb);
-                        process(ra, tile0 + 64 * h);
-                        __syncwarp();
-                        tmem_wait_ld(rb);
-                        if (h == 0) {
-                            tmem_ld32_async(tb + 64, ra);
-                        } else {
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(&ctl->t_empty[slot]);
-                        }
-                        process(rb, tile0 + 64 * h + 32);
-                        if (h == 0) {
-                            __syncwarp();
-                            tmem_wait_ld(ra);
-                        }
-                    }
-                } else {
-                    // registers are scarce at 4 M-tiles: one chunk at a time
-#pragma unroll 1
-                    for (int kc = 0; kc < 4; ++kc) {
-                        __syncwarp();
-                        tmem_ld32_async(tb + 32 * kc, ra);
-                        tmem_wait_ld(ra);
-                        if (kc == 3) {
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(&ctl->t_empty[slot]);
-                        }
-                        process(ra, tile0 + 32 * kc);
-                    }
-                }
-            }
-            if (!aborted && warp_rows)
-                while (b < b_end) finalize();
+            epilogue_warp<ARGMAX, INT8, C::kDoubleBuffer>(
+                p, row0 + mt * 128 + qd * 32, rows_total, tmem_base, qd, b_begin, b_end, t_begin, t_end,
+                n_tiles, ctl->t_full,
+                [&](int j) { return make_int2(mt + NMT * (j % (kSlots / NMT)), j / (kSlots / NMT)); },
+                [&](int slot) { mbar_arrive(&ctl->t_empty[slot]); }, abort_flag, false);
         }
     }
 
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

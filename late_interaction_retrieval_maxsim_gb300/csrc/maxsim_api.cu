@@ -95,14 +95,15 @@ maxsim_status_t encode_q(CUtensorMap *map, const void *Q, int n_q, int lq_max, i
 }
 
 // Rank-2 map over the packed D [total][128]: 16-bit -> boxes of 64 columns x
-// 128 tokens; int8 -> boxes of 128 columns x 128 tokens.  Rows past the end
-// read 0 and are masked by the kernel.
-maxsim_status_t encode_d(CUtensorMap *map, const void *D, int64_t total, maxsim_dtype_t dtype) {
+// box_rows tokens; int8 -> boxes of 128 columns x box_rows tokens.  Rows past
+// the end read 0 and are masked by the kernel.
+maxsim_status_t encode_d(CUtensorMap *map, const void *D, int64_t total, maxsim_dtype_t dtype,
+                         uint32_t box_rows) {
     const bool i8 = dtype == MAXSIM_INT8;
     const cuuint64_t esize = i8 ? 1 : 2;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(total)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDim) * esize};
-    cuuint32_t box[2] = {i8 ? 128u : 64u, 128u};
+    cuuint32_t box[2] = {i8 ? 128u : 64u, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUtensorMapDataType t = i8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                : (dtype == MAXSIM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -230,10 +231,12 @@ maxsim_status_t maxsim_forward(const void *Q, const int32_t *q_lens, int32_t n_q
     }
     alignas(64) CUtensorMap tmQ;
     alignas(64) CUtensorMap tmD;
-    if ((st = encode_q(&tmQ, q_src, n_q, lq_max, lq_pad, dtype == MAXSIM_BF16)) != MAXSIM_OK) return st;
-    if ((st = encode_d(&tmD, D, total_d_tokens, dtype)) != MAXSIM_OK) return st;
-
     const int nmt = forward_mtiles(rows);
+    if ((st = encode_q(&tmQ, q_src, n_q, lq_max, lq_pad, dtype == MAXSIM_BF16)) != MAXSIM_OK) return st;
+    if ((st = encode_d(&tmD, D, total_d_tokens, dtype, 128u)) != MAXSIM_OK) return st;
+
+    // Row groups of nmt * 128 padded rows; each group's documents are split
+    // into token-balanced parts, one CTA per (group, part).
     const int64_t groups = (rows + nmt * 128 - 1) / (nmt * 128);
     const int64_t parts = std::max<int64_t>(1, di.sm_count / groups);
     if (groups * parts > INT32_MAX) return MAXSIM_ERR_INVALID_ARGUMENT;
