@@ -14,9 +14,10 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - All array pointers are DEVICE pointers owned by the caller.  The library
- *    never allocates, frees or retains memory; scratch space is passed in as
- *    a caller-owned workspace whose size the matching *_workspace_size()
- *    call reports.
+ *    never allocates or frees memory; scratch space is passed in as a
+ *    caller-owned workspace whose size the matching *_workspace_size() call
+ *    reports (maxsim_forward_noalloc instead uses a fixed array the library
+ *    owns, see there).
  *  - Calls are stream-ordered and asynchronous: they enqueue work on
  *    `stream` (a cudaStream_t; NULL = the legacy default stream) and return.
  *    Outputs are valid once the stream has been synchronised.
@@ -112,6 +113,36 @@ maxsim_status_t maxsim_forward(const void *Q, const int32_t *q_lens, int32_t n_q
                                float q_scale, float d_scale,
                                float *scores, int64_t *raw_scores, int32_t *argmax,
                                void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * maxsim_forward for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart: this is a deployment convenience.  Some
+ * callers cannot call cudaMalloc where they score -- a plugin inside a host
+ * framework that owns every device allocation and gives its plugins no
+ * allocator, or a serving loop that must never allocate because cudaMalloc
+ * and cudaFree can synchronise the device and stall all of its streams.
+ * This entry point takes the same arguments as maxsim_forward minus the
+ * workspace and allocates nothing: the forward's scratch lives in one
+ * fixed 4 MiB array in device memory owned by the library (each GPU that
+ * loads the library holds it until the process exits).
+ *   - Sizes whose maxsim_forward_workspace_size() exceeds 4 MiB return
+ *     MAXSIM_ERR_WORKSPACE before anything is enqueued (4 MiB holds about
+ *     one million FP32 partial sums: e.g. a 1024-token query against
+ *     32,000 documents).
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call shares the one array and leaves its contents behind; calls
+ *     whose work overlaps on the GPU (other streams, other threads) race on
+ *     it and must be serialised by the caller.
+ */
+maxsim_status_t maxsim_forward_noalloc(const void *Q, const int32_t *q_lens, int32_t n_q, int32_t lq_max,
+                                       const void *D, const int32_t *cu_seqlens, int32_t n_docs,
+                                       int64_t total_d_tokens, int32_t dim, maxsim_dtype_t dtype,
+                                       float q_scale, float d_scale,
+                                       float *scores, int64_t *raw_scores, int32_t *argmax,
+                                       void *stream);
 
 /* Bytes of workspace maxsim_backward / maxsim_build_csr need. */
 size_t maxsim_backward_workspace_size(int32_t n_q, int32_t lq_max, int32_t n_docs,

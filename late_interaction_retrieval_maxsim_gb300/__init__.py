@@ -11,6 +11,7 @@ Entry points (same names as the C ABI):
   maxsim_forward   -- fused forward (FP16/BF16/INT8, dense or packed docs)
   maxsim_backward  -- dQ, dD from the saved argmax (inverse-grid CSR)
   maxsim_build_csr -- the inverse-grid CSR itself
+  maxsim_forward_noalloc -- the forward with library-owned scratch
   maxsim_device_status, maxsim_forward_workspace_size,
   maxsim_backward_workspace_size, maxsim_abi_version
 """
@@ -22,7 +23,7 @@ import os
 __all__ = [
     "load_library", "library_path", "maxsim_forward", "maxsim_backward", "maxsim_build_csr",
     "maxsim_device_status", "maxsim_forward_workspace_size", "maxsim_backward_workspace_size",
-    "maxsim_abi_version", "MaxSimError", "DTYPE_CODES",
+    "maxsim_abi_version", "maxsim_forward_noalloc", "MaxSimError", "DTYPE_CODES",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -70,6 +71,9 @@ def load_library():
     lib.maxsim_backward.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp, i32, i64, i32, ctypes.c_int,
                                     vp, vp, vp, sz, vp]
     lib.maxsim_backward.restype = ctypes.c_int
+    lib.maxsim_forward_noalloc.argtypes = [vp, vp, i32, i32, vp, vp, i32, i64, i32, ctypes.c_int, f32, f32,
+                                           vp, vp, vp, vp]
+    lib.maxsim_forward_noalloc.restype = ctypes.c_int
     lib.maxsim_device_status.argtypes = [vp, i32, ctypes.POINTER(i32)]
     lib.maxsim_device_status.restype = ctypes.c_int
     _LIB = lib
@@ -175,6 +179,31 @@ def maxsim_forward(Q, q_lens, D, cu_seqlens, *, with_argmax: bool = True, q_scal
                                 _ptr(raw_scores), _ptr(argmax), _ptr(workspace),
                                 workspace.numel() if workspace is not None else 0, _stream(stream))
     _check("maxsim_forward", st)
+    return scores, argmax, raw_scores
+
+
+def maxsim_forward_noalloc(Q, q_lens, D, cu_seqlens, scores, *, argmax=None, raw_scores=None,
+                           q_scale: float = 1.0, d_scale: float = 1.0, stream=None):
+    """C: ``maxsim_forward_noalloc`` -- maxsim_forward for callers that cannot
+    allocate device memory: the scratch lives in a fixed array owned by the
+    library, so only caller-provided outputs are written (``scores`` and the
+    optional ``argmax`` / ``raw_scores`` must be passed in).  Calls that
+    overlap on the GPU share that array and must be serialised."""
+    torch = _torch()
+    lib = load_library()
+    _require(Q, "Q")
+    dev = Q.device
+    _require(D, "D", dtype=Q.dtype, device=dev)
+    _require(q_lens, "q_lens", torch.int32, dev)
+    _require(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    _require(scores, "scores", torch.float32, dev)
+    n_q, lq_max, dim = Q.shape
+    with torch.cuda.device(dev):
+        st = lib.maxsim_forward_noalloc(_ptr(Q), _ptr(q_lens), n_q, lq_max, _ptr(D), _ptr(cu_seqlens),
+                                        cu_seqlens.numel() - 1, D.shape[0], dim, _dtype_code(Q),
+                                        float(q_scale), float(d_scale), _ptr(scores), _ptr(raw_scores),
+                                        _ptr(argmax), _stream(stream))
+    _check("maxsim_forward_noalloc", st)
     return scores, argmax, raw_scores
 
 
