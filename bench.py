@@ -63,9 +63,9 @@ def _peaks():
             "source": "fallback"}
 
 
-def _traffic(kernel_file: str, workload: str):
+def _traffic(workload: str):
     """DRAM bytes per launch from the committed ncu summary, when it was taken
-    on the current kernel source (else None)."""
+    on the current kernel sources (else None)."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
@@ -73,9 +73,10 @@ def _traffic(kernel_file: str, workload: str):
     rec = json.load(open(path)).get(workload)
     if not rec:
         return None
-    src = os.path.join(ROOT, "late_interaction_retrieval_maxsim_gb300", "csrc", kernel_file)
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    return rec["dram_bytes_per_launch"] if rec.get("source_sha256_16") == h else None
+    h = hashlib.sha256()
+    for f in rec["sources"]:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return rec["dram_bytes_per_launch"] if rec.get("source_sha256_16") == h.hexdigest()[:16] else None
 
 
 class ClockSampler:
@@ -290,7 +291,7 @@ def run_ours(args):
             "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
             "peak_source": f"{peaks['source']} bf16 burst (FP16 runs at the same dense rate)",
             "algorithmic_flops_per_launch": flops,
-            "traffic": _traffic("fwd_tc.cu", WORKLOAD),
+            "traffic": _traffic(WORKLOAD),
             "algorithmic_bytes_per_launch": rl.forward_hbm_bytes(w.n_q, w.lq, w.n_docs, total)}
 
     # end to end through the public API with host-resident inputs
