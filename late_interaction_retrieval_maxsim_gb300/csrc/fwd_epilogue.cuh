@@ -77,24 +77,37 @@ __device__ __forceinline__ bool fast_indicator_ok(float cm) {
 // finite difference.  Indicators are packed into the mask 8 at a time (sums
 // of distinct powers of two below 2^16 are exact in FP32).
 __device__ __forceinline__ uint32_t below_mask32(const uint32_t (&r)[32], float cm, bool fast) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    // acc[g] accumulates columns (16g + j, 16g + 8 + j), j = 0..7, with weight 2^j
+    // in its x / y lane: two indicators per packed FMA.
+    float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
     if (fast) {
         const float S = 0x1p100f;
         const float C = cm * S;
 #pragma unroll
-        for (int k = 0; k < 32; ++k)
-            acc[k >> 3] = fmaf(fma_sat(__uint_as_float(r[k]), -S, C), static_cast<float>(1u << (k & 7)),
-                               acc[k >> 3]);
+        for (int g = 0; g < 2; ++g)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float w = static_cast<float>(1u << j);
+                const float2 ind = make_float2(fma_sat(__uint_as_float(r[16 * g + j]), -S, C),
+                                               fma_sat(__uint_as_float(r[16 * g + 8 + j]), -S, C));
+                acc[g] = fma2(ind, make_float2(w, w), acc[g]);
+            }
     } else {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            const float t = cm - __uint_as_float(r[k]);
-            acc[k >> 3] = fmaf(mul_sat(mul_sat(t, 0x1p127f), 0x1p23f), static_cast<float>(1u << (k & 7)),
-                               acc[k >> 3]);
-        }
+        for (int g = 0; g < 2; ++g)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float w = static_cast<float>(1u << j);
+                const float t0 = cm - __uint_as_float(r[16 * g + j]);
+                const float t1 = cm - __uint_as_float(r[16 * g + 8 + j]);
+                const float2 ind = make_float2(mul_sat(mul_sat(t0, 0x1p127f), 0x1p23f),
+                                               mul_sat(mul_sat(t1, 0x1p127f), 0x1p23f));
+                acc[g] = fma2(ind, make_float2(w, w), acc[g]);
+            }
     }
-    const float lo = fmaf(acc[1], 256.f, acc[0]);
-    const float hi = fmaf(acc[3], 256.f, acc[2]);
+    // bits 0-7 / 8-15 of each half from the x / y lanes
+    const float lo = fmaf(acc[0].y, 256.f, acc[0].x);
+    const float hi = fmaf(acc[1].y, 256.f, acc[1].x);
     return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
