@@ -129,6 +129,27 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# --------------------------------------------------------------- multi-rank
+
+def rank_workload(w, rank: int):
+    """Weak scaling: every rank scores its own shard of the same shape, drawn
+    with a rank-specific seed (documents never move between ranks)."""
+    from late_interaction_retrieval_maxsim_gb300 import synthetic as syn
+    return syn.Workload(w.name, w.n_q, w.lq, w.n_docs, w.ld_lo, w.ld_hi, w.dtype, seed=w.seed + rank)
+
+
+def max_over_ranks(value: float, device) -> float:
+    """The slowest rank's time (the job finishes when it does); the only
+    collective of the benchmark, outside the timed region's data path."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # --------------------------------------------------------------------- ours
 
 def _time_loop(fn, steps, warmup, stream, nvtx=None):
@@ -251,8 +272,7 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     m.load_library()
     peaks = _peaks()
-    w = syn.WORKLOADS[WORKLOAD]
-    w = syn.Workload(w.name, w.n_q, w.lq, w.n_docs, w.ld_lo, w.ld_hi, w.dtype, seed=w.seed + rank)
+    w = rank_workload(syn.WORKLOADS[WORKLOAD], rank)
     x = syn.make_inputs(w, device="cuda")
     Q, ql, D, cu = x["Q"], x["q_lens"], x["D"], x["cu_seqlens"]
     total = D.shape[0]
@@ -274,11 +294,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         total_ms, per = _time_loop(step, args.steps, args.warmup, stream, nvtx="timed")
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, torch.device("cuda", local))
     if m.maxsim_device_status() != 0:
         raise RuntimeError("device status word set during the timed region")
 
