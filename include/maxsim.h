@@ -144,6 +144,59 @@ maxsim_status_t maxsim_forward_noalloc(const void *Q, const int32_t *q_lens, int
                                        float *scores, int64_t *raw_scores, int32_t *argmax,
                                        void *stream);
 
+/*
+ * Bytes of workspace maxsim_forward_host needs: two staging blocks of
+ * block_tokens document rows (double buffer), a device copy of the n_docs + 1
+ * offsets and the current block's rebased offsets, plus the forward's own
+ * scratch for block_docs documents.  Returns 0 for invalid sizes.
+ */
+size_t maxsim_forward_host_workspace_size(int32_t n_q, int32_t lq_max, int32_t n_docs, int32_t block_docs,
+                                          int64_t block_tokens, int32_t dim, maxsim_dtype_t dtype);
+
+/*
+ * Forward over a HOST-resident corpus: Flash-MaxSim §5 "Out-of-Core Corpus
+ * Scaling" (Table "Out-of-core scoring").  The fused forward's device
+ * footprint is one streamed block of documents, so a corpus larger than
+ * device memory is scored by keeping it in host memory and copying
+ * consecutive blocks of documents to the device, each block scored by the
+ * same kernels as maxsim_forward while the next block is copied.
+ *
+ *   Q, q_lens   DEVICE, as for maxsim_forward.
+ *   D_host      HOST [total_d_tokens, dim] packed rows.  For copy/compute
+ *               overlap it must be page-locked (cudaHostAlloc /
+ *               cudaHostRegister); pageable memory is accepted but its
+ *               copies stage through the driver and do not overlap.
+ *   cu_seqlens_host  HOST int32 [n_docs + 1] (cu[0] = 0, non-decreasing,
+ *               cu[n_docs] = total_d_tokens).  The call plans the blocks
+ *               from it and copies it to the workspace once, on `stream`.
+ *   scores, raw_scores, argmax   DEVICE, the same layouts and values as
+ *               maxsim_forward with the whole corpus resident; argmax and
+ *               raw_scores optional.
+ *   block_docs, block_tokens   Blocks are consecutive documents, greedily
+ *               as many as fit both limits; no document is split, so a
+ *               document longer than block_tokens is an argument error.
+ *   workspace   DEVICE, at least maxsim_forward_host_workspace_size() bytes.
+ *   stream      the stream every kernel runs on; the call's results are
+ *               complete when it has synchronised.
+ *   copy_stream a second stream for the host-to-device copies (NULL: the
+ *               copies go on `stream` and nothing overlaps).  It first waits
+ *               for the work already queued on `stream`.
+ * Scores are bit-identical to maxsim_forward's over the same corpus (a
+ * document's score does not depend on which other documents share a
+ * launch).  The call only enqueues; D_host and cu_seqlens_host must stay
+ * valid and unchanged until `stream` has synchronised.  Returns MAXSIM_OK, an argument error
+ * (nothing enqueued), or MAXSIM_ERR_CUDA (blocks before the failing one
+ * may have been enqueued).
+ */
+maxsim_status_t maxsim_forward_host(const void *Q, const int32_t *q_lens, int32_t n_q, int32_t lq_max,
+                                    const void *D_host, const int32_t *cu_seqlens_host, int32_t n_docs,
+                                    int64_t total_d_tokens, int32_t dim, maxsim_dtype_t dtype,
+                                    float q_scale, float d_scale,
+                                    float *scores, int64_t *raw_scores, int32_t *argmax,
+                                    int32_t block_docs, int64_t block_tokens,
+                                    void *workspace, size_t workspace_bytes, void *stream,
+                                    void *copy_stream);
+
 /* Bytes of workspace maxsim_backward / maxsim_build_csr need. */
 size_t maxsim_backward_workspace_size(int32_t n_q, int32_t lq_max, int32_t n_docs,
                                       int64_t total_d_tokens);

@@ -12,6 +12,8 @@ Entry points (same names as the C ABI):
   maxsim_backward  -- dQ, dD from the saved argmax (inverse-grid CSR)
   maxsim_build_csr -- the inverse-grid CSR itself
   maxsim_forward_noalloc -- the forward with library-owned scratch
+  maxsim_forward_host -- the forward over a host-resident corpus, streamed
+                         to the device in blocks (out-of-core scoring)
   maxsim_device_status, maxsim_forward_workspace_size,
   maxsim_backward_workspace_size, maxsim_abi_version
 """
@@ -23,7 +25,8 @@ import os
 __all__ = [
     "load_library", "library_path", "maxsim_forward", "maxsim_backward", "maxsim_build_csr",
     "maxsim_device_status", "maxsim_forward_workspace_size", "maxsim_backward_workspace_size",
-    "maxsim_abi_version", "maxsim_forward_noalloc", "MaxSimError", "DTYPE_CODES",
+    "maxsim_abi_version", "maxsim_forward_noalloc", "maxsim_forward_host",
+    "maxsim_forward_host_workspace_size", "MaxSimError", "DTYPE_CODES",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -74,6 +77,11 @@ def load_library():
     lib.maxsim_forward_noalloc.argtypes = [vp, vp, i32, i32, vp, vp, i32, i64, i32, ctypes.c_int, f32, f32,
                                            vp, vp, vp, vp]
     lib.maxsim_forward_noalloc.restype = ctypes.c_int
+    lib.maxsim_forward_host_workspace_size.argtypes = [i32, i32, i32, i32, i64, i32, ctypes.c_int]
+    lib.maxsim_forward_host_workspace_size.restype = sz
+    lib.maxsim_forward_host.argtypes = [vp, vp, i32, i32, vp, vp, i32, i64, i32, ctypes.c_int, f32, f32,
+                                        vp, vp, vp, i32, i64, vp, sz, vp, vp]
+    lib.maxsim_forward_host.restype = ctypes.c_int
     lib.maxsim_device_status.argtypes = [vp, i32, ctypes.POINTER(i32)]
     lib.maxsim_device_status.restype = ctypes.c_int
     _LIB = lib
@@ -204,6 +212,82 @@ def maxsim_forward_noalloc(Q, q_lens, D, cu_seqlens, scores, *, argmax=None, raw
                                         float(q_scale), float(d_scale), _ptr(scores), _ptr(raw_scores),
                                         _ptr(argmax), _stream(stream))
     _check("maxsim_forward_noalloc", st)
+    return scores, argmax, raw_scores
+
+
+def maxsim_forward_host_workspace_size(n_q: int, lq_max: int, n_docs: int, block_docs: int, block_tokens: int,
+                                       dtype, dim: int = 128) -> int:
+    code = DTYPE_CODES[dtype] if isinstance(dtype, str) else int(dtype)
+    return int(load_library().maxsim_forward_host_workspace_size(n_q, lq_max, n_docs, block_docs, block_tokens,
+                                                                 dim, code))
+
+
+_COPY_STREAMS = {}
+
+
+def _copy_stream_for(dev):
+    torch = _torch()
+    if dev not in _COPY_STREAMS:
+        _COPY_STREAMS[dev] = torch.cuda.Stream(device=dev)
+    return _COPY_STREAMS[dev]
+
+
+def maxsim_forward_host(Q, q_lens, D_host, cu_seqlens_host, *, block_docs: int, block_tokens: int = None,
+                        with_argmax: bool = False, q_scale: float = 1.0, d_scale: float = 1.0, scores=None,
+                        argmax=None, raw_scores=None, want_raw: bool = False, workspace=None,
+                        overlap: bool = True, copy_stream=None, stream=None):
+    """C: ``maxsim_forward_host`` -- out-of-core scoring: Q and q_lens on the
+    device, the corpus (D_host [total, 128], cu_seqlens_host [n_docs+1]
+    int32) in host memory.  Blocks of consecutive documents (at most
+    ``block_docs`` documents and ``block_tokens`` tokens) are copied to the
+    device on ``copy_stream`` (a cached side stream by default; the compute
+    stream when ``overlap`` is False) and scored while the next block is
+    copied.  D_host should be pinned (``tensor.pin_memory()``) for the
+    copies to overlap, and must stay alive and unchanged until ``stream``
+    has synchronised.  Returns device tensors like ``maxsim_forward``."""
+    torch = _torch()
+    lib = load_library()
+    _require(Q, "Q")
+    dev = Q.device
+    _require(q_lens, "q_lens", torch.int32, dev)
+    if not isinstance(D_host, torch.Tensor) or D_host.is_cuda or not D_host.is_contiguous():
+        raise ValueError("D_host must be a contiguous host tensor")
+    if D_host.dtype != Q.dtype:
+        raise TypeError(f"D_host must be {Q.dtype}, got {D_host.dtype}")
+    if (not isinstance(cu_seqlens_host, torch.Tensor) or cu_seqlens_host.is_cuda
+            or cu_seqlens_host.dtype != torch.int32 or not cu_seqlens_host.is_contiguous()):
+        raise ValueError("cu_seqlens_host must be a contiguous int32 host tensor")
+    if Q.dim() != 3 or D_host.dim() != 2 or Q.shape[2] != D_host.shape[1]:
+        raise ValueError("Q must be [n_q, lq_max, dim] and D_host [total, dim]")
+    n_q, lq_max, dim = Q.shape
+    n_docs = cu_seqlens_host.numel() - 1
+    total = D_host.shape[0]
+    code = _dtype_code(Q)
+    if block_tokens is None:
+        lens = cu_seqlens_host[1:] - cu_seqlens_host[:-1]
+        longest = int(lens.max()) if n_docs > 0 else 1
+        block_tokens = max(1, longest) * block_docs
+    if scores is None:
+        scores = torch.empty((n_q, n_docs), dtype=torch.float32, device=dev)
+    if with_argmax and argmax is None:
+        argmax = torch.empty((n_q, n_docs, lq_max), dtype=torch.int32, device=dev)
+    if not with_argmax:
+        argmax = None
+    if code == 2 and want_raw and raw_scores is None:
+        raw_scores = torch.empty((n_q, n_docs), dtype=torch.int64, device=dev)
+    ws_bytes = maxsim_forward_host_workspace_size(n_q, lq_max, n_docs, block_docs, block_tokens, code, dim)
+    if workspace is None or workspace.numel() < ws_bytes:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    if overlap and copy_stream is None:
+        copy_stream = _copy_stream_for(dev)
+    cs = ctypes.c_void_p(copy_stream.cuda_stream) if overlap else None
+    with torch.cuda.device(dev):
+        st = lib.maxsim_forward_host(_ptr(Q), _ptr(q_lens), n_q, lq_max, ctypes.c_void_p(D_host.data_ptr()),
+                                     ctypes.c_void_p(cu_seqlens_host.data_ptr()), n_docs, total, dim, code,
+                                     float(q_scale), float(d_scale), _ptr(scores), _ptr(raw_scores),
+                                     _ptr(argmax), int(block_docs), int(block_tokens), _ptr(workspace),
+                                     workspace.numel(), _stream(stream), cs)
+    _check("maxsim_forward_host", st)
     return scores, argmax, raw_scores
 
 

@@ -265,7 +265,7 @@ __device__ __forceinline__ void epilogue_warp(const FwdParams &p, int rho_warp, 
     // sum of row maxima over the query's tokens (fixed shuffle tree).
     auto finalize = [&]() {
         if (ARGMAX && row_valid)
-            p.argmax[(static_cast<int64_t>(q) * p.n_docs + b) * p.lq_max + i] =
+            p.argmax[(static_cast<int64_t>(q) * p.ld_out + b) * p.lq_max + i] =
                 (active && a >= 0) ? a - doc_lo : -1;
         if (INT8) {
             const bool empty_doc = doc_hi == doc_lo;
@@ -274,7 +274,7 @@ __device__ __forceinline__ void epilogue_warp(const FwdParams &p, int rho_warp, 
                 for (int off = 1; off < p.lq_pad; off <<= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
                 if (i == 0 && q < p.n_q) {
                     const bool neg_inf = empty_doc && qlen > 0;
-                    const int64_t idx = static_cast<int64_t>(q) * p.n_docs + b;
+                    const int64_t idx = static_cast<int64_t>(q) * p.ld_out + b;
                     if (p.raw_scores) p.raw_scores[idx] = neg_inf ? INT64_MIN : c;
                     p.scores[idx] = neg_inf ? -INFINITY
                                             : static_cast<float>(static_cast<double>(c) * p.int8_scale);
@@ -289,10 +289,10 @@ __device__ __forceinline__ void epilogue_warp(const FwdParams &p, int rho_warp, 
             if (p.lq_pad == 32) {
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
-                if (lane == 0 && q < p.n_q) p.scores[static_cast<int64_t>(q) * p.n_docs + b] = c;
+                if (lane == 0 && q < p.n_q) p.scores[static_cast<int64_t>(q) * p.ld_out + b] = c;
             } else if (p.lq_pad < 32) {
                 for (int off = 1; off < p.lq_pad; off <<= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
-                if (i == 0 && q < p.n_q) p.scores[static_cast<int64_t>(q) * p.n_docs + b] = c;
+                if (i == 0 && q < p.n_q) p.scores[static_cast<int64_t>(q) * p.ld_out + b] = c;
             } else {
                 for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
                 if (lane == 0 && q < p.n_q)

@@ -287,18 +287,19 @@ __global__ void finalize_partials_kernel(FwdParams p, int n_chunks, bool int8) {
     const int64_t n_pairs = static_cast<int64_t>(p.n_q) * p.n_docs;
     for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n_pairs;
          idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int q = static_cast<int>(idx / p.n_docs);
+        const int b = static_cast<int>(idx - static_cast<int64_t>(q) * p.n_docs);
+        const int64_t out = static_cast<int64_t>(q) * p.ld_out + b;
         if (int8) {
-            const int q = static_cast<int>(idx / p.n_docs);
-            const int b = static_cast<int>(idx - static_cast<int64_t>(q) * p.n_docs);
             long long s = 0;
             for (int c = 0; c < n_chunks; ++c) s += p.ipartials[c * n_pairs + idx];
             const bool neg_inf = p.cu_seqlens[b + 1] == p.cu_seqlens[b] && p.q_lens[q] > 0;
-            if (p.raw_scores) p.raw_scores[idx] = neg_inf ? INT64_MIN : s;
-            p.scores[idx] = neg_inf ? -INFINITY : static_cast<float>(static_cast<double>(s) * p.int8_scale);
+            if (p.raw_scores) p.raw_scores[out] = neg_inf ? INT64_MIN : s;
+            p.scores[out] = neg_inf ? -INFINITY : static_cast<float>(static_cast<double>(s) * p.int8_scale);
         } else {
             float s = 0.0f;
             for (int c = 0; c < n_chunks; ++c) s += p.partials[c * n_pairs + idx];
-            p.scores[idx] = s;
+            p.scores[out] = s;
         }
     }
 }
@@ -310,11 +311,13 @@ __global__ void fill_empty_kernel(FwdParams p, bool int8) {
     for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n_pairs;
          idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int q = static_cast<int>(idx / p.n_docs);
+        const int b = static_cast<int>(idx - static_cast<int64_t>(q) * p.n_docs);
+        const int64_t out = static_cast<int64_t>(q) * p.ld_out + b;
         const bool has = p.q_lens[q] > 0;
-        p.scores[idx] = has ? -INFINITY : 0.0f;
-        if (int8 && p.raw_scores) p.raw_scores[idx] = has ? INT64_MIN : 0;
+        p.scores[out] = has ? -INFINITY : 0.0f;
+        if (int8 && p.raw_scores) p.raw_scores[out] = has ? INT64_MIN : 0;
         if (p.argmax)
-            for (int i = 0; i < p.lq_max; ++i) p.argmax[idx * p.lq_max + i] = -1;
+            for (int i = 0; i < p.lq_max; ++i) p.argmax[out * p.lq_max + i] = -1;
     }
 }
 
@@ -381,6 +384,20 @@ cudaError_t launch_fill_empty(const FwdParams &p, bool int8, cudaStream_t stream
     const int64_t n = static_cast<int64_t>(p.n_q) * p.n_docs;
     if (n == 0) return cudaSuccess;
     fill_empty_kernel<<<grid_for(n, 256), 256, 0, stream>>>(p, int8);
+    return cudaGetLastError();
+}
+
+// Offsets of a block of documents [b0, b0 + n) of a larger corpus, rebased
+// so the block reads as a corpus of its own: dst[k] = src[k] - src[0] for
+// k = 0 .. n, with src = corpus offsets + b0.
+__global__ void rebase_offsets_kernel(const int32_t *src, int32_t *dst, int32_t n) {
+    const int32_t base = src[0];
+    for (int32_t k = blockIdx.x * blockDim.x + threadIdx.x; k <= n; k += gridDim.x * blockDim.x)
+        dst[k] = src[k] - base;
+}
+
+cudaError_t launch_rebase_offsets(const int32_t *src, int32_t *dst, int32_t n, cudaStream_t stream) {
+    rebase_offsets_kernel<<<grid_for(static_cast<int64_t>(n) + 1, 256), 256, 0, stream>>>(src, dst, n);
     return cudaGetLastError();
 }
 

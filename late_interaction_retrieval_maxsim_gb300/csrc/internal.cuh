@@ -16,14 +16,15 @@ namespace maxsim {
 struct FwdParams {
     const int32_t *q_lens;
     const int32_t *cu_seqlens;
-    float *scores;       // [n_q, n_docs]
+    float *scores;       // [n_q, ld_out], columns [0, n_docs) written
     float *partials;     // [lq_pad / 32, n_q, n_docs] when lq_pad > 32
     int64_t *ipartials;  // INT8: [lq_pad / 32, n_q, n_docs] int64 when lq_pad > 32
-    int64_t *raw_scores; // INT8 only, may be null
-    int32_t *argmax;     // [n_q, n_docs, lq_max] or null
+    int64_t *raw_scores; // INT8 only, may be null; [n_q, ld_out]
+    int32_t *argmax;     // [n_q, ld_out, lq_max] or null
     int32_t *status;     // device status word
     int32_t n_q, lq_max, lq_pad, n_docs;
     int32_t total_tokens;
+    int64_t ld_out;         // documents per output row (>= n_docs)
     int32_t groups, parts;  // grid = groups * parts CTAs
     uint32_t idesc;         // tcgen05 instruction descriptor
     double int8_scale;      // (double)q_scale * (double)d_scale
@@ -40,6 +41,7 @@ cudaError_t launch_forward(const CUtensorMap &tmQ, const CUtensorMap &tmD, const
 cudaError_t launch_finalize_partials(const FwdParams &p, bool int8, cudaStream_t stream);
 cudaError_t launch_fill_empty(const FwdParams &p, bool int8, cudaStream_t stream);
 cudaError_t launch_int8_to_f16(const int8_t *src, uint16_t *dst, int64_t n, cudaStream_t stream);
+cudaError_t launch_rebase_offsets(const int32_t *src, int32_t *dst, int32_t n, cudaStream_t stream);
 
 // bwd.cu
 struct BwdParams {

@@ -14,6 +14,7 @@
 #include <cstdint>
 #include <mutex>
 #include <unordered_map>
+#include <vector>
 
 namespace maxsim {
 
@@ -145,6 +146,175 @@ BwdLayout backward_layout(int32_t n_q, int32_t lq_max, int32_t n_docs, int64_t t
     return l;
 }
 
+// Staging layout of maxsim_forward_host: two D blocks (double buffer), the
+// corpus's offsets copied once, the current block's rebased offsets, one
+// set of per-chunk partials (the forwards run in order on one stream) and
+// the FP16 copy of an INT8 Q.
+struct HostLayout {
+    size_t stage_off[2] = {0, 0};
+    size_t cu_all_off = 0, cu_block_off = 0, partials_off = 0, q16_off = 0, total = 0;
+};
+
+HostLayout host_layout(int32_t n_q, int32_t lq_max, int32_t n_docs, int32_t block_docs, int64_t block_tokens,
+                       maxsim_dtype_t dtype) {
+    HostLayout h;
+    const size_t stage = align_up(static_cast<size_t>(block_tokens) * kDim * (dtype == MAXSIM_INT8 ? 1 : 2));
+    const FwdLayout f = forward_layout(n_q, std::max(lq_max, 1), block_docs, dtype);
+    size_t off = 0;
+    h.stage_off[0] = off;
+    off += stage;
+    h.stage_off[1] = off;
+    off += stage;
+    h.cu_all_off = off;
+    off += align_up(static_cast<size_t>(n_docs + 1) * sizeof(int32_t));
+    h.cu_block_off = off;
+    off += align_up(static_cast<size_t>(block_docs + 1) * sizeof(int32_t));
+    h.partials_off = off;
+    off += f.partials;
+    h.q16_off = off;
+    off += f.q16;
+    h.total = off;
+    return h;
+}
+
+// Greedy split of documents [0, n_docs) into consecutive blocks; starts gets
+// the first document of each block followed by n_docs.
+maxsim_status_t plan_host_blocks(const int32_t *cu, int32_t n_docs, int64_t total, int32_t block_docs,
+                                 int64_t block_tokens, std::vector<int32_t> &starts) {
+    if (cu[0] != 0 || cu[n_docs] != total) return MAXSIM_ERR_INVALID_ARGUMENT;
+    starts.clear();
+    starts.push_back(0);
+    int32_t b0 = 0;
+    for (int32_t b = 0; b < n_docs; ++b) {
+        const int64_t len = static_cast<int64_t>(cu[b + 1]) - cu[b];
+        if (len < 0 || len > block_tokens) return MAXSIM_ERR_INVALID_ARGUMENT;
+        if (b - b0 == block_docs || static_cast<int64_t>(cu[b + 1]) - cu[b0] > block_tokens) {
+            starts.push_back(b);
+            b0 = b;
+        }
+    }
+    starts.push_back(n_docs);
+    return MAXSIM_OK;
+}
+
+// Events of one maxsim_forward_host call; destroyed when the call returns
+// (the runtime releases an event still pending once the device reaches it).
+struct EventSet {
+    cudaEvent_t start = nullptr, copied[2] = {nullptr, nullptr}, computed[2] = {nullptr, nullptr};
+    cudaError_t create(bool needed) {
+        if (!needed) return cudaSuccess;
+        for (cudaEvent_t *e : {&start, &copied[0], &copied[1], &computed[0], &computed[1]}) {
+            cudaError_t r = cudaEventCreateWithFlags(e, cudaEventDisableTiming);
+            if (r != cudaSuccess) return r;
+        }
+        return cudaSuccess;
+    }
+    ~EventSet() {
+        for (cudaEvent_t e : {start, copied[0], copied[1], computed[0], computed[1]})
+            if (e) cudaEventDestroy(e);
+    }
+};
+
+maxsim_status_t check_forward_args(const void *Q, const int32_t *q_lens, int32_t n_q, int32_t lq_max,
+                                   int32_t n_docs, int64_t total_d_tokens, int32_t dim, maxsim_dtype_t dtype,
+                                   float q_scale, float d_scale) {
+    if (dtype != MAXSIM_FP16 && dtype != MAXSIM_BF16 && dtype != MAXSIM_INT8) return MAXSIM_ERR_UNSUPPORTED;
+    if (dim != kDim) return MAXSIM_ERR_UNSUPPORTED;
+    if (n_q < 0 || n_docs < 0 || lq_max < 0 || total_d_tokens < 0) return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (total_d_tokens > INT32_MAX - 256) return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (n_q == 0 || n_docs == 0) return MAXSIM_OK;
+    if (!q_lens) return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (lq_max > 0 && (!Q || !aligned16(Q))) return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (dtype == MAXSIM_INT8 && !(q_scale > 0.0f && d_scale > 0.0f)) return MAXSIM_ERR_INVALID_ARGUMENT;
+    const int64_t rows = static_cast<int64_t>(n_q) * (lq_max > 0 ? lq_padded(lq_max) : 1);
+    if (rows > INT32_MAX / 2 || static_cast<int64_t>(n_q) * n_docs * std::max(1, lq_max) > INT64_MAX / 8)
+        return MAXSIM_ERR_INVALID_ARGUMENT;
+    return MAXSIM_OK;
+}
+
+// What a forward over any set of documents shares: the query side (its
+// tensor map, the FP16 widening of an INT8 Q), the tile configuration and
+// the partial-sum scratch.
+struct ForwardPlan {
+    FwdParams p{};
+    alignas(64) CUtensorMap tmQ;
+    int nmt = 1;
+    int sm_count = 0;
+    bool int8 = false, empty_q = false;
+    maxsim_dtype_t dtype = MAXSIM_FP16;
+};
+
+maxsim_status_t forward_prepare(ForwardPlan &plan, const void *Q, const int32_t *q_lens, int32_t n_q,
+                                int32_t lq_max, maxsim_dtype_t dtype, float q_scale, float d_scale,
+                                uint8_t *partials, uint8_t *q16_scratch,
+                                cudaStream_t stream) {
+    DeviceInfo di;
+    maxsim_status_t st = device_info(&di);
+    if (st != MAXSIM_OK) return st;
+    const bool int8 = dtype == MAXSIM_INT8;
+    const int lq_pad = lq_max > 0 ? lq_padded(lq_max) : 1;
+    FwdParams &p = plan.p;
+    p.q_lens = q_lens;
+    p.status = di.status;
+    p.n_q = n_q;
+    p.lq_max = lq_max;
+    p.lq_pad = lq_pad;
+    p.int8_scale = int8 ? static_cast<double>(q_scale) * static_cast<double>(d_scale) : 0.0;
+    if (lq_pad > 32) {
+        if (int8) p.ipartials = reinterpret_cast<int64_t *>(partials);
+        else p.partials = reinterpret_cast<float *>(partials);
+    }
+    p.idesc = ptx::idesc_f16(dtype == MAXSIM_BF16, 128, 128);
+    plan.int8 = int8;
+    plan.dtype = dtype;
+    plan.sm_count = di.sm_count;
+    plan.empty_q = lq_max == 0;
+    plan.nmt = forward_mtiles(static_cast<int64_t>(n_q) * lq_pad);
+    if (plan.empty_q) return MAXSIM_OK;
+    const void *q_src = Q;
+    if (int8) {
+        uint16_t *q16 = reinterpret_cast<uint16_t *>(q16_scratch);
+        if (launch_int8_to_f16(static_cast<const int8_t *>(Q), q16, static_cast<int64_t>(n_q) * lq_max * kDim,
+                               stream) != cudaSuccess)
+            return MAXSIM_ERR_CUDA;
+        q_src = q16;
+    }
+    return encode_q(&plan.tmQ, q_src, n_q, lq_max, lq_pad, dtype == MAXSIM_BF16);
+}
+
+// One forward over documents [0, n_docs) of (D, cu_seqlens) whose outputs
+// land in columns [0, n_docs) of rows of ld_out documents.
+maxsim_status_t forward_block(ForwardPlan &plan, const void *D, const int32_t *cu_seqlens, int32_t n_docs,
+                              int64_t total, float *scores, int64_t *raw_scores, int32_t *argmax,
+                              int64_t ld_out, cudaStream_t stream) {
+    FwdParams p = plan.p;
+    p.cu_seqlens = cu_seqlens;
+    p.scores = scores;
+    p.raw_scores = plan.int8 ? raw_scores : nullptr;
+    p.argmax = argmax;
+    p.n_docs = n_docs;
+    p.total_tokens = static_cast<int32_t>(total);
+    p.ld_out = ld_out;
+    if (n_docs == 0) return MAXSIM_OK;
+    if (total == 0 || plan.empty_q) return cuda_status(launch_fill_empty(p, plan.int8, stream));
+
+    alignas(64) CUtensorMap tmD;
+    maxsim_status_t st = encode_d(&tmD, D, total, plan.dtype, 128u);
+    if (st != MAXSIM_OK) return st;
+    // Row groups of nmt * 128 padded rows; each group's documents are split
+    // into token-balanced parts, one CTA per (group, part).
+    const int64_t rows = static_cast<int64_t>(p.n_q) * p.lq_pad;
+    const int64_t groups = (rows + plan.nmt * 128 - 1) / (plan.nmt * 128);
+    const int64_t parts = std::max<int64_t>(1, plan.sm_count / groups);
+    if (groups * parts > INT32_MAX) return MAXSIM_ERR_INVALID_ARGUMENT;
+    p.groups = static_cast<int32_t>(groups);
+    p.parts = static_cast<int32_t>(parts);
+    cudaError_t e = launch_forward(plan.tmQ, tmD, p, plan.nmt, argmax != nullptr, plan.int8, stream);
+    if (e != cudaSuccess) return MAXSIM_ERR_CUDA;
+    if (p.lq_pad > 32) return cuda_status(launch_finalize_partials(p, plan.int8, stream));
+    return MAXSIM_OK;
+}
+
 }  // namespace
 }  // namespace maxsim
 
@@ -179,76 +349,110 @@ maxsim_status_t maxsim_forward(const void *Q, const int32_t *q_lens, int32_t n_q
                                int32_t *argmax, void *workspace, size_t workspace_bytes,
                                void *stream_) {
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-    if (dtype != MAXSIM_FP16 && dtype != MAXSIM_BF16 && dtype != MAXSIM_INT8) return MAXSIM_ERR_UNSUPPORTED;
-    if (dim != kDim) return MAXSIM_ERR_UNSUPPORTED;
-    if (n_q < 0 || n_docs < 0 || lq_max < 0 || total_d_tokens < 0) return MAXSIM_ERR_INVALID_ARGUMENT;
-    if (total_d_tokens > INT32_MAX - 256) return MAXSIM_ERR_INVALID_ARGUMENT;
+    maxsim_status_t st = check_forward_args(Q, q_lens, n_q, lq_max, n_docs, total_d_tokens, dim, dtype,
+                                            q_scale, d_scale);
+    if (st != MAXSIM_OK) return st;
     if (n_q == 0 || n_docs == 0) return MAXSIM_OK;
-    if (!q_lens || !cu_seqlens || !scores) return MAXSIM_ERR_INVALID_ARGUMENT;
-    if (lq_max > 0 && (!Q || !aligned16(Q))) return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (!cu_seqlens || !scores) return MAXSIM_ERR_INVALID_ARGUMENT;
     if (total_d_tokens > 0 && (!D || !aligned16(D))) return MAXSIM_ERR_INVALID_ARGUMENT;
-    if (dtype == MAXSIM_INT8 && !(q_scale > 0.0f && d_scale > 0.0f)) return MAXSIM_ERR_INVALID_ARGUMENT;
-    const int lq_pad = lq_max > 0 ? lq_padded(lq_max) : 1;
-    const int64_t rows = static_cast<int64_t>(n_q) * lq_pad;
-    if (rows > INT32_MAX / 2 || static_cast<int64_t>(n_q) * n_docs * std::max(1, lq_max) > INT64_MAX / 8)
-        return MAXSIM_ERR_INVALID_ARGUMENT;
     const FwdLayout wl = forward_layout(n_q, lq_max, n_docs, dtype);
     if (wl.total > 0 && (workspace == nullptr || workspace_bytes < wl.total)) return MAXSIM_ERR_WORKSPACE;
 
-    DeviceInfo di;
-    maxsim_status_t st = device_info(&di);
+    ForwardPlan plan;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    st = forward_prepare(plan, Q, q_lens, n_q, lq_max, dtype, q_scale, d_scale, ws, ws + wl.partials,
+                         stream);
+    if (st != MAXSIM_OK) return st;
+    return forward_block(plan, D, cu_seqlens, n_docs, total_d_tokens, scores, raw_scores, argmax, n_docs,
+                         stream);
+}
+
+size_t maxsim_forward_host_workspace_size(int32_t n_q, int32_t lq_max, int32_t n_docs, int32_t block_docs,
+                                          int64_t block_tokens, int32_t dim, maxsim_dtype_t dtype) {
+    (void)dim;
+    if (n_q <= 0 || lq_max < 0 || n_docs < 0 || block_docs <= 0 || block_tokens <= 0) return 0;
+    return host_layout(n_q, lq_max, n_docs, block_docs, block_tokens, dtype).total;
+}
+
+maxsim_status_t maxsim_forward_host(const void *Q, const int32_t *q_lens, int32_t n_q, int32_t lq_max,
+                                    const void *D_host, const int32_t *cu_seqlens_host, int32_t n_docs,
+                                    int64_t total_d_tokens, int32_t dim, maxsim_dtype_t dtype,
+                                    float q_scale, float d_scale, float *scores, int64_t *raw_scores,
+                                    int32_t *argmax, int32_t block_docs, int64_t block_tokens,
+                                    void *workspace, size_t workspace_bytes, void *stream_,
+                                    void *copy_stream_) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    cudaStream_t copy_stream = copy_stream_ ? static_cast<cudaStream_t>(copy_stream_) : stream;
+    maxsim_status_t st = check_forward_args(Q, q_lens, n_q, lq_max, n_docs, total_d_tokens, dim, dtype,
+                                            q_scale, d_scale);
+    if (st != MAXSIM_OK) return st;
+    if (block_docs <= 0 || block_tokens <= 0 || block_tokens > INT32_MAX - 256)
+        return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (n_q == 0 || n_docs == 0) return MAXSIM_OK;
+    if (!cu_seqlens_host || !scores) return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (total_d_tokens > 0 && !D_host) return MAXSIM_ERR_INVALID_ARGUMENT;
+
+    // Plan on the host: consecutive documents, at most block_docs documents
+    // and block_tokens tokens per block; a document never straddles blocks.
+    std::vector<int32_t> starts;
+    st = plan_host_blocks(cu_seqlens_host, n_docs, total_d_tokens, block_docs, block_tokens, starts);
     if (st != MAXSIM_OK) return st;
 
-    const bool int8 = dtype == MAXSIM_INT8;
-    FwdParams p{};
-    p.q_lens = q_lens;
-    p.cu_seqlens = cu_seqlens;
-    p.scores = scores;
-    p.raw_scores = int8 ? raw_scores : nullptr;
-    p.argmax = argmax;
-    p.status = di.status;
-    p.n_q = n_q;
-    p.lq_max = lq_max;
-    p.lq_pad = lq_pad;
-    p.n_docs = n_docs;
-    p.total_tokens = static_cast<int32_t>(total_d_tokens);
-    p.int8_scale = int8 ? static_cast<double>(q_scale) * static_cast<double>(d_scale) : 0.0;
+    const HostLayout hl = host_layout(n_q, lq_max, n_docs, block_docs, block_tokens, dtype);
+    if (workspace == nullptr || workspace_bytes < hl.total) return MAXSIM_ERR_WORKSPACE;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    if (wl.partials) {
-        if (int8) p.ipartials = reinterpret_cast<int64_t *>(ws);
-        else p.partials = reinterpret_cast<float *>(ws);
-    }
 
-    if (total_d_tokens == 0 || lq_max == 0) return cuda_status(launch_fill_empty(p, int8, stream));
+    ForwardPlan plan;
+    st = forward_prepare(plan, Q, q_lens, n_q, lq_max, dtype, q_scale, d_scale, ws + hl.partials_off,
+                         ws + hl.q16_off, stream);
+    if (st != MAXSIM_OK) return st;
 
-    const void *q_src = Q;
-    if (int8) {
-        uint16_t *q16 = reinterpret_cast<uint16_t *>(ws + wl.partials);
-        cudaError_t e = launch_int8_to_f16(static_cast<const int8_t *>(Q), q16,
-                                           static_cast<int64_t>(n_q) * lq_max * kDim, stream);
-        if (e != cudaSuccess) return MAXSIM_ERR_CUDA;
-        q_src = q16;
-    }
-    alignas(64) CUtensorMap tmQ;
-    alignas(64) CUtensorMap tmD;
-    const int nmt = forward_mtiles(rows);
-    if ((st = encode_q(&tmQ, q_src, n_q, lq_max, lq_pad, dtype == MAXSIM_BF16)) != MAXSIM_OK) return st;
-    if ((st = encode_d(&tmD, D, total_d_tokens, dtype, 128u)) != MAXSIM_OK) return st;
-
-    // Row groups of nmt * 128 padded rows; each group's documents are split
-    // into token-balanced parts, one CTA per (group, part).
-    const int64_t groups = (rows + nmt * 128 - 1) / (nmt * 128);
-    const int64_t parts = std::max<int64_t>(1, di.sm_count / groups);
-    if (groups * parts > INT32_MAX) return MAXSIM_ERR_INVALID_ARGUMENT;
-    p.groups = static_cast<int32_t>(groups);
-    p.parts = static_cast<int32_t>(parts);
-    p.idesc = ptx::idesc_f16(dtype == MAXSIM_BF16, 128, 128);
-
-    cudaError_t e = launch_forward(tmQ, tmD, p, nmt, argmax != nullptr, int8, stream);
+    // The offsets go to the device once, ordered before every block on the
+    // compute stream; each block's rebased slice is made there by a kernel.
+    int32_t *cu_all = reinterpret_cast<int32_t *>(ws + hl.cu_all_off);
+    int32_t *cu_block = reinterpret_cast<int32_t *>(ws + hl.cu_block_off);
+    cudaError_t e = cudaMemcpyAsync(cu_all, cu_seqlens_host, static_cast<size_t>(n_docs + 1) * sizeof(int32_t),
+                                    cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess) return MAXSIM_ERR_CUDA;
-    if (lq_pad > 32) {
-        e = launch_finalize_partials(p, int8, stream);
-        if (e != cudaSuccess) return MAXSIM_ERR_CUDA;
+
+    const size_t row_bytes = static_cast<size_t>(kDim) * (dtype == MAXSIM_INT8 ? 1 : 2);
+    const char *d_host = static_cast<const char *>(D_host);
+    EventSet ev;
+    if (ev.create(copy_stream != stream) != cudaSuccess) return MAXSIM_ERR_CUDA;
+    if (copy_stream != stream) {
+        // The copies may overwrite staging buffers only after whatever the
+        // compute stream had queued before this call.
+        if ((e = cudaEventRecord(ev.start, stream)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(copy_stream, ev.start, 0)) != cudaSuccess)
+            return MAXSIM_ERR_CUDA;
+    }
+    const int n_blocks = static_cast<int>(starts.size()) - 1;
+    for (int k = 0; k < n_blocks; ++k) {
+        const int slot = k & 1;
+        const int32_t b0 = starts[k], b1 = starts[k + 1];
+        const int32_t nb = b1 - b0;
+        const int64_t t0 = cu_seqlens_host[b0], t1 = cu_seqlens_host[b1];
+        uint8_t *d_stage = ws + hl.stage_off[slot];
+        // Staging slot k & 1 is free once block k - 2's forward has run.
+        if (copy_stream != stream && k >= 2 &&
+            (e = cudaStreamWaitEvent(copy_stream, ev.computed[slot], 0)) != cudaSuccess)
+            return MAXSIM_ERR_CUDA;
+        if (t1 > t0 && (e = cudaMemcpyAsync(d_stage, d_host + static_cast<size_t>(t0) * row_bytes,
+                                            static_cast<size_t>(t1 - t0) * row_bytes,
+                                            cudaMemcpyHostToDevice, copy_stream)) != cudaSuccess)
+            return MAXSIM_ERR_CUDA;
+        if (copy_stream != stream) {
+            if ((e = cudaEventRecord(ev.copied[slot], copy_stream)) != cudaSuccess ||
+                (e = cudaStreamWaitEvent(stream, ev.copied[slot], 0)) != cudaSuccess)
+                return MAXSIM_ERR_CUDA;
+        }
+        if ((e = launch_rebase_offsets(cu_all + b0, cu_block, nb, stream)) != cudaSuccess) return MAXSIM_ERR_CUDA;
+        st = forward_block(plan, d_stage, cu_block, nb, t1 - t0, scores + b0,
+                           raw_scores ? raw_scores + b0 : nullptr,
+                           argmax ? argmax + static_cast<int64_t>(b0) * lq_max : nullptr, n_docs, stream);
+        if (st != MAXSIM_OK) return st;
+        if (copy_stream != stream && (e = cudaEventRecord(ev.computed[slot], stream)) != cudaSuccess)
+            return MAXSIM_ERR_CUDA;
     }
     return MAXSIM_OK;
 }

@@ -85,3 +85,37 @@ def test_argument_errors_return_before_touching_the_device(lib):
              vp(16), vp(16), None, 0, None) == 3                  # no workspace
     c = lib.maxsim_build_csr
     assert c(vp(16), vp(16), 1, 32, vp(16), 1, 10, None, vp(16), vp(16), 1 << 20, None) == 1
+
+
+def test_host_corpus_argument_errors_return_before_touching_the_device(lib):
+    """maxsim_forward_host plans its blocks on the host; plan errors and a
+    short workspace return before any CUDA call."""
+    vp = ctypes.c_void_p
+    lib.maxsim_forward_host.argtypes = [vp, vp, ctypes.c_int32, ctypes.c_int32, vp, vp, ctypes.c_int32,
+                                        ctypes.c_int64, ctypes.c_int32, ctypes.c_int, ctypes.c_float,
+                                        ctypes.c_float, vp, vp, vp, ctypes.c_int32, ctypes.c_int64, vp,
+                                        ctypes.c_size_t, vp, vp]
+    lib.maxsim_forward_host_workspace_size.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                                       ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
+                                                       ctypes.c_int]
+    lib.maxsim_forward_host_workspace_size.restype = ctypes.c_size_t
+    cu = (ctypes.c_int32 * 4)(0, 5, 40, 41)
+    cu_bad = (ctypes.c_int32 * 4)(1, 5, 40, 41)
+    host = vp(ctypes.addressof(cu))
+
+    def call(cu_arr, block_docs, block_tokens, ws_bytes, total=41, dim=128):
+        return lib.maxsim_forward_host(vp(16), vp(16), 1, 32, host, vp(ctypes.addressof(cu_arr)), 3, total, dim,
+                                       0, 1.0, 1.0, vp(16), None, None, block_docs, block_tokens, vp(256),
+                                       ws_bytes, None, None)
+
+    need = lib.maxsim_forward_host_workspace_size(1, 32, 3, 2, 64, 128, 0)
+    # two staging blocks of 64 rows x 256 B plus the corpus's and a block's offsets
+    assert need >= 2 * 64 * 256 + 4 * 4 + 3 * 4
+    assert call(cu, 2, 64, need, dim=64) == 2          # dim != 128
+    assert call(cu, 0, 64, need) == 1                  # no documents per block
+    assert call(cu, 2, 0, need) == 1                   # no tokens per block
+    assert call(cu, 2, 34, need) == 1                  # document 1 has 35 tokens
+    assert call(cu_bad, 2, 64, need) == 1              # cu[0] != 0
+    assert call(cu, 2, 64, need, total=40) == 1        # cu[n_docs] != total
+    assert call(cu, 2, 64, need - 1) == 3              # workspace too small
+    assert lib.maxsim_forward_host_workspace_size(1, 32, 3, 0, 64, 128, 0) == 0
