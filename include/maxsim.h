@@ -145,6 +145,96 @@ maxsim_status_t maxsim_forward_noalloc(const void *Q, const int32_t *q_lens, int
                                        void *stream);
 
 /*
+ * INT8 x INT8 forward with one symmetric scale per TOKEN: Flash-MaxSim
+ * §4.3.1 "INT8xINT8 Quantization" (per-token quantisation of both Q and D,
+ * dequantisation fused into the kernel).  For each valid query row i and
+ * document token t the kernel forms the exact integer dot product
+ * dot(i, t) = <Q[q, i, :], D[cu[b] + t, :]> and ranks
+ *     v(i, t) = fp32( (float)dot(i, t) * d_scales[cu[b] + t] )
+ * (one IEEE single-precision product: dot is an integer below 2^24, so
+ * (float)dot is exact); the row maximum m_i = max_t v(i, t) and its lowest
+ * attaining t (the argmax) are taken on these FP32 values, then
+ *     scores[q, b] = sum_{i < q_lens[q]} fp32(q_scales[q, i] * m_i)
+ * in FP32 in a fixed order (a document with no tokens gives -inf).  The
+ * query scale multiplies after the maximum, which selects the same token as
+ * scaling before it when the scale is positive.
+ *   Q           int8 [n_q, lq_max, dim], values in [-127, 127] (device).
+ *   q_scales    FP32 [n_q, lq_max], finite and >= 0 (device).
+ *   D           int8 [total_d_tokens, dim] packed (device).
+ *   d_scales    FP32 [total_d_tokens], finite and >= 0 (device).
+ *   scores, argmax   as maxsim_forward (argmax optional).
+ *   workspace   maxsim_forward_workspace_size(n_q, lq_max, n_docs, dim,
+ *               MAXSIM_INT8) bytes.
+ * Unlike the per-tensor INT8 path the result is not an exact integer: the
+ * page's own description calls the per-token path approximate.
+ */
+maxsim_status_t maxsim_forward_int8_per_token(const int8_t *Q, const float *q_scales, const int32_t *q_lens,
+                                              int32_t n_q, int32_t lq_max, const int8_t *D,
+                                              const float *d_scales, const int32_t *cu_seqlens,
+                                              int32_t n_docs, int64_t total_d_tokens, int32_t dim,
+                                              float *scores, int32_t *argmax,
+                                              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Row-wise top-K selection, the selection step of the two-stage scan below.
+ * For each of n_rows rows of `values` (FP32, row stride ld >= n_cols), the
+ * k largest entries in descending order; equal values are ordered by
+ * ascending column, so the result is unique.  out_ids / out_values: [n_rows,
+ * k]; positions past n_cols (k > n_cols) get id -1 and value -inf.  -inf
+ * ranks below every finite value; NaN inputs give unspecified results.
+ * k <= 4096 (larger: MAXSIM_ERR_UNSUPPORTED).  One CTA per row.
+ */
+maxsim_status_t maxsim_topk(const float *values, int32_t n_rows, int32_t n_cols, int64_t ld, int32_t k,
+                            int32_t *out_ids, float *out_values, void *stream);
+
+/* Bytes of workspace maxsim_rerank_two_stage needs. */
+size_t maxsim_rerank_workspace_size(int32_t n_q, int32_t lq_max, int32_t n_docs, int32_t k_candidates,
+                                    int32_t max_doc_len, int32_t dim, maxsim_dtype_t dtype16);
+
+/*
+ * Two-stage INT8 -> FP16 top-K scan: Flash-MaxSim §4.1 "Kernel Family" lists
+ * it among the forward variants without further detail; the reading taken:
+ *   1. every document is scored against every query with the INT8 MaxSim
+ *      (maxsim_forward with MAXSIM_INT8 and one scale per tensor, or
+ *      maxsim_forward_int8_per_token when q_tok_scales and d_tok_scales are
+ *      both given);
+ *   2. each query keeps its k_candidates best documents (maxsim_topk order:
+ *      ties to the lower document index);
+ *   3. those candidates' rows are gathered from the FP16/BF16 copy of the
+ *      corpus and rescored against the query's FP16/BF16 tokens with the
+ *      fused forward (FP32 accumulation);
+ *   4. each query returns its k best candidates by the stage-3 score
+ *      (ties to the earlier candidate).
+ *   Q8, D8, q_lens, cu_seqlens   the INT8 query/corpus (device), layouts as
+ *               maxsim_forward; q_scale, d_scale the per-tensor scales
+ *               (ignored in per-token mode).
+ *   Q16         FP16/BF16 [n_q, lq_max, dim] (device), the same queries.
+ *   D16         FP16/BF16 [total_d_tokens, dim], the same corpus: device
+ *               memory, or page-locked host memory (cudaHostAlloc /
+ *               cudaHostRegister) that the gather reads over the host link;
+ *               pageable memory is an argument error.  Only candidates'
+ *               rows are read.
+ *   max_doc_len the longest document (sizes the gather buffer); a longer
+ *               candidate is cut to max_doc_len rows and sets the device
+ *               status word (code 0x202).
+ *   top_ids, top_scores   [n_q, k] (device): document ids and their stage-3
+ *               FP32 scores; -1 / -inf past the number of documents.
+ *   candidate_ids  optional [n_q, k_candidates] (device): stage-2 ids.
+ *   workspace   maxsim_rerank_workspace_size() bytes (device): holds the
+ *               stage-1 scores [n_q, n_docs] and n_q * k_candidates *
+ *               max_doc_len gathered rows.
+ * 1 <= k_candidates <= 4096, 0 <= k <= k_candidates.
+ */
+maxsim_status_t maxsim_rerank_two_stage(const int8_t *Q8, const float *q_tok_scales, float q_scale,
+                                        const int8_t *D8, const float *d_tok_scales, float d_scale,
+                                        const void *Q16, const void *D16, maxsim_dtype_t dtype16,
+                                        const int32_t *q_lens, int32_t n_q, int32_t lq_max,
+                                        const int32_t *cu_seqlens, int32_t n_docs, int64_t total_d_tokens,
+                                        int32_t max_doc_len, int32_t dim, int32_t k_candidates, int32_t k,
+                                        int32_t *top_ids, float *top_scores, int32_t *candidate_ids,
+                                        void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Bytes of workspace maxsim_forward_host needs: two staging blocks of
  * block_tokens document rows (double buffer), a device copy of the n_docs + 1
  * offsets and the current block's rebased offsets, plus the forward's own

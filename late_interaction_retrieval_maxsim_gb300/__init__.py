@@ -14,6 +14,9 @@ Entry points (same names as the C ABI):
   maxsim_forward_noalloc -- the forward with library-owned scratch
   maxsim_forward_host -- the forward over a host-resident corpus, streamed
                          to the device in blocks (out-of-core scoring)
+  maxsim_forward_int8_per_token -- INT8 forward with one scale per token
+  maxsim_topk      -- row-wise top-K selection (ties to the lower column)
+  maxsim_rerank_two_stage -- INT8 scan, top-K' candidates, FP16 rescoring
   maxsim_device_status, maxsim_forward_workspace_size,
   maxsim_backward_workspace_size, maxsim_abi_version
 """
@@ -26,7 +29,8 @@ __all__ = [
     "load_library", "library_path", "maxsim_forward", "maxsim_backward", "maxsim_build_csr",
     "maxsim_device_status", "maxsim_forward_workspace_size", "maxsim_backward_workspace_size",
     "maxsim_abi_version", "maxsim_forward_noalloc", "maxsim_forward_host",
-    "maxsim_forward_host_workspace_size", "MaxSimError", "DTYPE_CODES",
+    "maxsim_forward_host_workspace_size", "maxsim_forward_int8_per_token", "maxsim_topk",
+    "maxsim_rerank_two_stage", "maxsim_rerank_workspace_size", "MaxSimError", "DTYPE_CODES",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -82,6 +86,16 @@ def load_library():
     lib.maxsim_forward_host.argtypes = [vp, vp, i32, i32, vp, vp, i32, i64, i32, ctypes.c_int, f32, f32,
                                         vp, vp, vp, i32, i64, vp, sz, vp, vp]
     lib.maxsim_forward_host.restype = ctypes.c_int
+    lib.maxsim_forward_int8_per_token.argtypes = [vp, vp, vp, i32, i32, vp, vp, vp, i32, i64, i32, vp, vp,
+                                                  vp, sz, vp]
+    lib.maxsim_forward_int8_per_token.restype = ctypes.c_int
+    lib.maxsim_topk.argtypes = [vp, i32, i32, i64, i32, vp, vp, vp]
+    lib.maxsim_topk.restype = ctypes.c_int
+    lib.maxsim_rerank_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.c_int]
+    lib.maxsim_rerank_workspace_size.restype = sz
+    lib.maxsim_rerank_two_stage.argtypes = [vp, vp, f32, vp, vp, f32, vp, vp, ctypes.c_int, vp, i32, i32, vp,
+                                            i32, i64, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
+    lib.maxsim_rerank_two_stage.restype = ctypes.c_int
     lib.maxsim_device_status.argtypes = [vp, i32, ctypes.POINTER(i32)]
     lib.maxsim_device_status.restype = ctypes.c_int
     _LIB = lib
@@ -289,6 +303,114 @@ def maxsim_forward_host(Q, q_lens, D_host, cu_seqlens_host, *, block_docs: int, 
                                      workspace.numel(), _stream(stream), cs)
     _check("maxsim_forward_host", st)
     return scores, argmax, raw_scores
+
+
+def maxsim_forward_int8_per_token(Q, q_scales, q_lens, D, d_scales, cu_seqlens, *, with_argmax: bool = True,
+                                  scores=None, argmax=None, workspace=None, stream=None):
+    """C: ``maxsim_forward_int8_per_token`` -- INT8 MaxSim with one scale
+    per token: Q int8 [n_q, lq_max, 128] with q_scales float32 [n_q,
+    lq_max]; D int8 [total, 128] with d_scales float32 [total].  Returns
+    (scores [n_q, n_docs] float32, argmax or None)."""
+    torch = _torch()
+    lib = load_library()
+    _require(Q, "Q", torch.int8)
+    dev = Q.device
+    _require(D, "D", torch.int8, dev)
+    _require(q_scales, "q_scales", torch.float32, dev)
+    _require(d_scales, "d_scales", torch.float32, dev)
+    _require(q_lens, "q_lens", torch.int32, dev)
+    _require(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    n_q, lq_max, dim = Q.shape
+    n_docs = cu_seqlens.numel() - 1
+    if q_scales.shape != (n_q, lq_max) or d_scales.shape != (D.shape[0],):
+        raise ValueError("q_scales must be [n_q, lq_max] and d_scales [total]")
+    if scores is None:
+        scores = torch.empty((n_q, n_docs), dtype=torch.float32, device=dev)
+    if with_argmax and argmax is None:
+        argmax = torch.empty((n_q, n_docs, lq_max), dtype=torch.int32, device=dev)
+    if not with_argmax:
+        argmax = None
+    ws_bytes = maxsim_forward_workspace_size(n_q, lq_max, n_docs, 2, dim)
+    if ws_bytes and (workspace is None or workspace.numel() < ws_bytes):
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.maxsim_forward_int8_per_token(_ptr(Q), _ptr(q_scales), _ptr(q_lens), n_q, lq_max, _ptr(D),
+                                               _ptr(d_scales), _ptr(cu_seqlens), n_docs, D.shape[0], dim,
+                                               _ptr(scores), _ptr(argmax), _ptr(workspace),
+                                               workspace.numel() if workspace is not None else 0,
+                                               _stream(stream))
+    _check("maxsim_forward_int8_per_token", st)
+    return scores, argmax
+
+
+def maxsim_topk(values, k: int, *, out_ids=None, out_values=None, stream=None):
+    """C: ``maxsim_topk`` -- per row of values [n_rows, n_cols] (float32,
+    CUDA; rows may be strided), the k largest entries, descending, ties to
+    the lower column.  Returns (ids int32 [n_rows, k], values [n_rows, k])."""
+    torch = _torch()
+    lib = load_library()
+    if values.dim() != 2 or values.dtype != torch.float32 or not values.is_cuda or values.stride(1) != 1:
+        raise ValueError("values must be a float32 CUDA matrix with unit column stride")
+    n_rows, n_cols = values.shape
+    dev = values.device
+    if out_ids is None:
+        out_ids = torch.empty((n_rows, k), dtype=torch.int32, device=dev)
+    if out_values is None:
+        out_values = torch.empty((n_rows, k), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.maxsim_topk(_ptr(values), n_rows, n_cols, values.stride(0) if n_rows > 1 else n_cols, k,
+                             _ptr(out_ids), _ptr(out_values), _stream(stream))
+    _check("maxsim_topk", st)
+    return out_ids, out_values
+
+
+def maxsim_rerank_workspace_size(n_q: int, lq_max: int, n_docs: int, k_candidates: int, max_doc_len: int,
+                                 dtype16, dim: int = 128) -> int:
+    code = DTYPE_CODES[dtype16] if isinstance(dtype16, str) else int(dtype16)
+    return int(load_library().maxsim_rerank_workspace_size(n_q, lq_max, n_docs, k_candidates, max_doc_len, dim,
+                                                           code))
+
+
+def maxsim_rerank_two_stage(Q8, D8, Q16, D16, q_lens, cu_seqlens, *, k_candidates: int, k: int,
+                            q_scale: float = 1.0, d_scale: float = 1.0, q_tok_scales=None, d_tok_scales=None,
+                            max_doc_len: int = None, workspace=None, return_candidates: bool = False,
+                            stream=None):
+    """C: ``maxsim_rerank_two_stage`` -- INT8 scan of every document, the
+    k_candidates best per query rescored with the FP16/BF16 tokens, the k
+    best returned.  D16 may be a CUDA tensor or a pinned host tensor (the
+    gather then reads the candidates' rows over the host link).  Returns
+    (ids int32 [n_q, k], scores float32 [n_q, k], candidate ids or None)."""
+    torch = _torch()
+    lib = load_library()
+    _require(Q8, "Q8", torch.int8)
+    dev = Q8.device
+    _require(D8, "D8", torch.int8, dev)
+    _require(Q16, "Q16", None, dev)
+    _require(q_lens, "q_lens", torch.int32, dev)
+    _require(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    if D16.is_cuda:
+        _require(D16, "D16", Q16.dtype, dev)
+    elif not (D16.is_pinned() and D16.is_contiguous() and D16.dtype == Q16.dtype):
+        raise ValueError("a host D16 must be a contiguous pinned tensor of Q16's dtype")
+    n_q, lq_max, dim = Q8.shape
+    n_docs = cu_seqlens.numel() - 1
+    code16 = _dtype_code(Q16)
+    if max_doc_len is None:
+        max_doc_len = int((cu_seqlens[1:] - cu_seqlens[:-1]).max()) if n_docs else 0
+    ws_bytes = maxsim_rerank_workspace_size(n_q, lq_max, n_docs, k_candidates, max_doc_len, code16, dim)
+    if workspace is None or workspace.numel() < ws_bytes:
+        workspace = torch.empty(max(1, ws_bytes), dtype=torch.uint8, device=dev)
+    ids = torch.empty((n_q, k), dtype=torch.int32, device=dev)
+    scores = torch.empty((n_q, k), dtype=torch.float32, device=dev)
+    cand = torch.empty((n_q, k_candidates), dtype=torch.int32, device=dev) if return_candidates else None
+    with torch.cuda.device(dev):
+        st = lib.maxsim_rerank_two_stage(
+            _ptr(Q8), _ptr(q_tok_scales), float(q_scale), _ptr(D8), _ptr(d_tok_scales), float(d_scale),
+            _ptr(Q16), ctypes.c_void_p(D16.data_ptr()), code16, _ptr(q_lens), n_q, lq_max, _ptr(cu_seqlens),
+            n_docs, D8.shape[0], max_doc_len, dim, k_candidates, k, _ptr(ids), _ptr(scores), _ptr(cand),
+            _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("maxsim_rerank_two_stage", st)
+    return ids, scores, cand
 
 
 def maxsim_build_csr(argmax, q_lens, cu_seqlens, total_d_tokens: int, *, workspace=None, stream=None):

@@ -225,8 +225,11 @@ __device__ __forceinline__ void fold_split(const uint32_t (&r)[32], int c0, int 
 // slot_of(j).y), reads the 128 columns 32 at a time, hands the slot back
 // with release(slot) once the last chunk is in registers, and folds the
 // chunks into the running maxima; at each document end it writes the argmax
-// row and the (partial) score.  DB double-buffers the TMEM reads.
-template <bool ARGMAX, bool INT8, bool DB, typename SlotOf, typename Release>
+// row and the (partial) score.  DB double-buffers the TMEM reads.  INT8 sums
+// the (integer) maxima in int64; SCALE multiplies each column by its
+// document token's scale before the maximum and the row maximum by the
+// query token's scale, then sums in FP32.
+template <bool ARGMAX, bool INT8, bool SCALE, bool DB, typename SlotOf, typename Release>
 __device__ __forceinline__ void epilogue_warp(const FwdParams &p, int rho_warp, int64_t rows_total,
                                               uint32_t tmem_base, int qd, int b_begin, int b_end,
                                               int t_begin, int t_end, int n_tiles, uint64_t *t_full,
@@ -241,6 +244,19 @@ __device__ __forceinline__ void epilogue_warp(const FwdParams &p, int rho_warp, 
     const int qlen = (q < p.n_q) ? p.q_lens[q] : 0;
     const bool active = row_valid && i < qlen;
     const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
+    [[maybe_unused]] const float q_scale = (SCALE && active) ? p.q_tok_scale[q * p.lq_max + i] : 0.0f;
+
+    // SCALE: lane l holds the scale of column c0 + l of the next chunk (0
+    // past this CTA's tokens); every column of the row is multiplied by its
+    // scale, broadcast by shuffles.
+    auto chunk_scale = [&](int c0) -> float {
+        return (SCALE && c0 + lane < t_end) ? __ldg(p.d_tok_scale + c0 + lane) : 0.0f;
+    };
+    auto apply_scale = [&](uint32_t (&r)[32], float s) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+            r[k] = __float_as_uint(__uint_as_float(r[k]) * __shfl_sync(0xffffffffu, s, k));
+    };
 
     // Upcoming document boundaries: lane l holds cu[cu_base + l]; one
     // coalesced load serves 32 documents, read back by shuffles.
@@ -286,6 +302,7 @@ __device__ __forceinline__ void epilogue_warp(const FwdParams &p, int rho_warp, 
             }
         } else {
             float c = active ? m : 0.0f;
+            if (SCALE && active && m != -INFINITY) c = m * q_scale;
             if (p.lq_pad == 32) {
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
@@ -361,14 +378,18 @@ __device__ __forceinline__ void epilogue_warp(const FwdParams &p, int rho_warp, 
         const int tile0 = t_begin + j * kBlockN;
         if constexpr (DB) {
             // four 32-column chunks, the next one loading while one is folded
+            [[maybe_unused]] float sa = chunk_scale(tile0), sb = 0.0f;
             __syncwarp();
             tmem_ld32_async(tb, ra);
             tmem_wait_ld(ra);
+            if constexpr (SCALE) apply_scale(ra, sa);
 #pragma unroll 1
             for (int h = 0; h < 2; ++h) {
+                if constexpr (SCALE) sb = chunk_scale(tile0 + 64 * h + 32);
                 __syncwarp();
                 tmem_ld32_async(tb + 64 * h + 32, rb);
                 process(ra, tile0 + 64 * h);
+                if constexpr (SCALE) if (h == 0) sa = chunk_scale(tile0 + 64);
                 __syncwarp();
                 tmem_wait_ld(rb);
                 if (h == 0) {
@@ -378,16 +399,19 @@ __device__ __forceinline__ void epilogue_warp(const FwdParams &p, int rho_warp, 
                     __syncwarp();
                     if (lane == 0) release(slot);
                 }
+                if constexpr (SCALE) apply_scale(rb, sb);
                 process(rb, tile0 + 64 * h + 32);
                 if (h == 0) {
                     __syncwarp();
                     tmem_wait_ld(ra);
+                    if constexpr (SCALE) apply_scale(ra, sa);
                 }
             }
         } else {
             // registers are scarce at 4 M-tiles: one chunk at a time
 #pragma unroll 1
             for (int kc = 0; kc < 4; ++kc) {
+                [[maybe_unused]] const float sc = chunk_scale(tile0 + 32 * kc);
                 __syncwarp();
                 tmem_ld32_async(tb + 32 * kc, ra);
                 tmem_wait_ld(ra);
@@ -396,6 +420,7 @@ __device__ __forceinline__ void epilogue_warp(const FwdParams &p, int rho_warp, 
                     __syncwarp();
                     if (lane == 0) release(slot);
                 }
+                if constexpr (SCALE) apply_scale(ra, sc);
                 process(ra, tile0 + 32 * kc);
             }
         }

@@ -5,7 +5,8 @@
 // similarity sub-tile on chip, fold it into a running row maximum (§4.1.1,
 // masking positions outside the document to -inf before the reduction), and
 // write one scalar per (query, document) pair; padding-free packed documents
-// per §4.3.2; INT8 x INT8 per §4.3.1 (one scale per tensor).
+// per §4.3.2; INT8 x INT8 per §4.3.1 (one scale per tensor, or one per
+// token).
 //
 // GB300 design (differs from the pages' one-program-per-pair scheme):
 //  * One CTA owns up to 4 M-tiles of 128 padded query rows (all queries of a
@@ -25,7 +26,10 @@
 //  * INT8: a converter warp-set widens each int8 tile to FP16 in shared
 //    memory (exact: |x| <= 127) for the same FP16 MMA; every product and
 //    partial sum is an integer below 2^24, so the FP32 accumulator holds the
-//    exact int32 dot product, and sums over query tokens run in int64.
+//    exact int32 dot product, and sums over query tokens run in int64.  With
+//    one scale per token the epilogue multiplies each exact dot product by
+//    its document token's scale (FP32) before the row maximum and the
+//    maximum by the query token's scale, and sums in FP32.
 #include "internal.cuh"
 #include "sm103.cuh"
 #include "fwd_epilogue.cuh"
@@ -89,7 +93,7 @@ __device__ __forceinline__ uint2 widen_i8x4(uint32_t w) {
     return make_uint2(*reinterpret_cast<uint32_t *>(&l), *reinterpret_cast<uint32_t *>(&h));
 }
 
-template <int NMT, bool ARGMAX, bool INT8>
+template <int NMT, bool ARGMAX, bool INT8, bool SCALE>
 __global__ void __launch_bounds__(Cfg<NMT, INT8>::kThreads, 1)
 maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmD,
                   const FwdParams p) {
@@ -127,8 +131,9 @@ maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         mbar_init(&ctl->mma_done, 1);
         fence_mbar_init();
         ctl->abort = 0;
-        // token-balanced contiguous document range of this part
-        const int64_t T = p.total_tokens;
+        // token-balanced contiguous document range of this part (the token
+        // count is read from the offsets: the tensor map may extend past it)
+        const int64_t T = p.cu_seqlens[p.n_docs];
         const int64_t lo = T * part / p.parts;
         const int64_t hi = T * (part + 1) / p.parts;
         const int bb = lower_bound_cu(p.cu_seqlens, p.n_docs, lo);
@@ -266,7 +271,7 @@ maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         const int mt = (warp - C::kFirstEpiWarp) >> 2;
         const int qd = warp & 3;  // TMEM lane quarter this warp may access
         if (mt < n_mt) {
-            epilogue_warp<ARGMAX, INT8, C::kDoubleBuffer>(
+            epilogue_warp<ARGMAX, INT8 && !SCALE, SCALE, C::kDoubleBuffer>(
                 p, row0 + mt * 128 + qd * 32, rows_total, tmem_base, qd, b_begin, b_end, t_begin, t_end,
                 n_tiles, ctl->t_full,
                 [&](int j) { return make_int2(mt + NMT * (j % (kSlots / NMT)), j / (kSlots / NMT)); },
@@ -327,24 +332,24 @@ __global__ void int8_to_f16_kernel(const int8_t *__restrict__ src, __half *__res
         dst[k] = __int2half_rn(static_cast<int>(src[k]));
 }
 
-template <int NMT, bool ARGMAX, bool INT8>
+template <int NMT, bool ARGMAX, bool INT8, bool SCALE>
 cudaError_t launch_one(const CUtensorMap &tmQ, const CUtensorMap &tmD, const FwdParams &p,
                        cudaStream_t stream) {
     using C = Cfg<NMT, INT8>;
-    auto kern = maxsim_fwd_kernel<NMT, ARGMAX, INT8>;
+    auto kern = maxsim_fwd_kernel<NMT, ARGMAX, INT8, SCALE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     kern<<<p.groups * p.parts, C::kThreads, C::kSmem, stream>>>(tmQ, tmD, p);
     return cudaGetLastError();
 }
 
-template <bool ARGMAX, bool INT8>
+template <bool ARGMAX, bool INT8, bool SCALE>
 cudaError_t launch_nmt(int nmt, const CUtensorMap &tmQ, const CUtensorMap &tmD, const FwdParams &p,
                        cudaStream_t stream) {
     switch (nmt) {
-        case 1: return launch_one<1, ARGMAX, INT8>(tmQ, tmD, p, stream);
-        case 2: return launch_one<2, ARGMAX, INT8>(tmQ, tmD, p, stream);
-        default: return launch_one<4, ARGMAX, INT8>(tmQ, tmD, p, stream);
+        case 1: return launch_one<1, ARGMAX, INT8, SCALE>(tmQ, tmD, p, stream);
+        case 2: return launch_one<2, ARGMAX, INT8, SCALE>(tmQ, tmD, p, stream);
+        default: return launch_one<4, ARGMAX, INT8, SCALE>(tmQ, tmD, p, stream);
     }
 }
 
@@ -365,12 +370,18 @@ int forward_threads(int nmt, bool int8) {
 }
 
 cudaError_t launch_forward(const CUtensorMap &tmQ, const CUtensorMap &tmD, const FwdParams &p,
-                           int nmt, bool with_argmax, bool int8, cudaStream_t stream) {
-    if (int8)
-        return with_argmax ? launch_nmt<true, true>(nmt, tmQ, tmD, p, stream)
-                           : launch_nmt<false, true>(nmt, tmQ, tmD, p, stream);
-    return with_argmax ? launch_nmt<true, false>(nmt, tmQ, tmD, p, stream)
-                       : launch_nmt<false, false>(nmt, tmQ, tmD, p, stream);
+                           int nmt, bool with_argmax, FwdMode mode, cudaStream_t stream) {
+    switch (mode) {
+        case FwdMode::kInt8Tensor:
+            return with_argmax ? launch_nmt<true, true, false>(nmt, tmQ, tmD, p, stream)
+                               : launch_nmt<false, true, false>(nmt, tmQ, tmD, p, stream);
+        case FwdMode::kInt8Token:
+            return with_argmax ? launch_nmt<true, true, true>(nmt, tmQ, tmD, p, stream)
+                               : launch_nmt<false, true, true>(nmt, tmQ, tmD, p, stream);
+        default:
+            return with_argmax ? launch_nmt<true, false, false>(nmt, tmQ, tmD, p, stream)
+                               : launch_nmt<false, false, false>(nmt, tmQ, tmD, p, stream);
+    }
 }
 
 cudaError_t launch_finalize_partials(const FwdParams &p, bool int8, cudaStream_t stream) {

@@ -21,6 +21,8 @@ struct FwdParams {
     int64_t *ipartials;  // INT8: [lq_pad / 32, n_q, n_docs] int64 when lq_pad > 32
     int64_t *raw_scores; // INT8 only, may be null; [n_q, ld_out]
     int32_t *argmax;     // [n_q, ld_out, lq_max] or null
+    const float *q_tok_scale;  // INT8 per-token mode: [n_q, lq_max] query-token scales
+    const float *d_tok_scale;  // INT8 per-token mode: [total_tokens] document-token scales
     int32_t *status;     // device status word
     int32_t n_q, lq_max, lq_pad, n_docs;
     int32_t total_tokens;
@@ -36,12 +38,28 @@ inline int forward_mtiles(int64_t rows) { return rows <= 128 ? 1 : rows <= 256 ?
 // fwd_tc.cu
 int forward_smem_bytes(int nmt, bool int8);
 int forward_threads(int nmt, bool int8);
+// Forward arithmetic: FP16/BF16 MMA on the inputs; INT8 with one scale per
+// tensor (exact integer maxima, int64 sums); INT8 with one scale per token
+// (exact integer dots scaled per document token in FP32 before the maximum,
+// per query token after it, FP32 sums).
+enum class FwdMode { kF16 = 0, kInt8Tensor = 1, kInt8Token = 2 };
 cudaError_t launch_forward(const CUtensorMap &tmQ, const CUtensorMap &tmD, const FwdParams &p,
-                           int nmt, bool with_argmax, bool int8, cudaStream_t stream);
+                           int nmt, bool with_argmax, FwdMode mode, cudaStream_t stream);
 cudaError_t launch_finalize_partials(const FwdParams &p, bool int8, cudaStream_t stream);
 cudaError_t launch_fill_empty(const FwdParams &p, bool int8, cudaStream_t stream);
 cudaError_t launch_int8_to_f16(const int8_t *src, uint16_t *dst, int64_t n, cudaStream_t stream);
 cudaError_t launch_rebase_offsets(const int32_t *src, int32_t *dst, int32_t n, cudaStream_t stream);
+
+// topk.cu
+constexpr int kTopkMax = 4096;  // largest k a row-wise top-K selection takes
+cudaError_t launch_topk(const float *values, int64_t ld, int32_t n_rows, int32_t n_cols, int32_t k,
+                        const int32_t *col_ids, int64_t ld_ids, int32_t *out_ids, float *out_values,
+                        cudaStream_t stream);
+cudaError_t launch_candidate_offsets(const int32_t *cand, int32_t n_q, int32_t n_cand, const int32_t *cu,
+                                     int32_t max_len, int32_t *cand_cu, int32_t *status, cudaStream_t stream);
+cudaError_t launch_gather_candidates(const int32_t *cand, int32_t n_q, int32_t n_cand, const int32_t *cu,
+                                     const int32_t *cand_cu, const void *src, int64_t row_bytes, void *dst,
+                                     int64_t slice_rows, int sm_count, cudaStream_t stream);
 
 // bwd.cu
 struct BwdParams {

@@ -241,13 +241,14 @@ struct ForwardPlan {
     int nmt = 1;
     int sm_count = 0;
     bool int8 = false, empty_q = false;
+    FwdMode mode = FwdMode::kF16;
     maxsim_dtype_t dtype = MAXSIM_FP16;
 };
 
 maxsim_status_t forward_prepare(ForwardPlan &plan, const void *Q, const int32_t *q_lens, int32_t n_q,
                                 int32_t lq_max, maxsim_dtype_t dtype, float q_scale, float d_scale,
-                                uint8_t *partials, uint8_t *q16_scratch,
-                                cudaStream_t stream) {
+                                uint8_t *partials, uint8_t *q16_scratch, cudaStream_t stream,
+                                const float *q_tok_scale = nullptr) {
     DeviceInfo di;
     maxsim_status_t st = device_info(&di);
     if (st != MAXSIM_OK) return st;
@@ -260,8 +261,10 @@ maxsim_status_t forward_prepare(ForwardPlan &plan, const void *Q, const int32_t 
     p.lq_max = lq_max;
     p.lq_pad = lq_pad;
     p.int8_scale = int8 ? static_cast<double>(q_scale) * static_cast<double>(d_scale) : 0.0;
+    plan.mode = !int8 ? FwdMode::kF16 : q_tok_scale ? FwdMode::kInt8Token : FwdMode::kInt8Tensor;
+    p.q_tok_scale = q_tok_scale;
     if (lq_pad > 32) {
-        if (int8) p.ipartials = reinterpret_cast<int64_t *>(partials);
+        if (plan.mode == FwdMode::kInt8Tensor) p.ipartials = reinterpret_cast<int64_t *>(partials);
         else p.partials = reinterpret_cast<float *>(partials);
     }
     p.idesc = ptx::idesc_f16(dtype == MAXSIM_BF16, 128, 128);
@@ -283,20 +286,24 @@ maxsim_status_t forward_prepare(ForwardPlan &plan, const void *Q, const int32_t 
 }
 
 // One forward over documents [0, n_docs) of (D, cu_seqlens) whose outputs
-// land in columns [0, n_docs) of rows of ld_out documents.
+// land in columns [0, n_docs) of rows of ld_out documents.  `total` sizes the
+// tensor map over D and may exceed cu_seqlens[n_docs] (the kernels balance
+// work by the offsets themselves).
 maxsim_status_t forward_block(ForwardPlan &plan, const void *D, const int32_t *cu_seqlens, int32_t n_docs,
                               int64_t total, float *scores, int64_t *raw_scores, int32_t *argmax,
-                              int64_t ld_out, cudaStream_t stream) {
+                              int64_t ld_out, cudaStream_t stream, const float *d_tok_scale = nullptr) {
+    const bool int64_sums = plan.mode == FwdMode::kInt8Tensor;
     FwdParams p = plan.p;
     p.cu_seqlens = cu_seqlens;
+    p.d_tok_scale = d_tok_scale;
     p.scores = scores;
-    p.raw_scores = plan.int8 ? raw_scores : nullptr;
+    p.raw_scores = int64_sums ? raw_scores : nullptr;
     p.argmax = argmax;
     p.n_docs = n_docs;
     p.total_tokens = static_cast<int32_t>(total);
     p.ld_out = ld_out;
     if (n_docs == 0) return MAXSIM_OK;
-    if (total == 0 || plan.empty_q) return cuda_status(launch_fill_empty(p, plan.int8, stream));
+    if (total == 0 || plan.empty_q) return cuda_status(launch_fill_empty(p, int64_sums, stream));
 
     alignas(64) CUtensorMap tmD;
     maxsim_status_t st = encode_d(&tmD, D, total, plan.dtype, 128u);
@@ -309,10 +316,41 @@ maxsim_status_t forward_block(ForwardPlan &plan, const void *D, const int32_t *c
     if (groups * parts > INT32_MAX) return MAXSIM_ERR_INVALID_ARGUMENT;
     p.groups = static_cast<int32_t>(groups);
     p.parts = static_cast<int32_t>(parts);
-    cudaError_t e = launch_forward(plan.tmQ, tmD, p, plan.nmt, argmax != nullptr, plan.int8, stream);
+    cudaError_t e = launch_forward(plan.tmQ, tmD, p, plan.nmt, argmax != nullptr, plan.mode, stream);
     if (e != cudaSuccess) return MAXSIM_ERR_CUDA;
-    if (p.lq_pad > 32) return cuda_status(launch_finalize_partials(p, plan.int8, stream));
+    if (p.lq_pad > 32) return cuda_status(launch_finalize_partials(p, int64_sums, stream));
     return MAXSIM_OK;
+}
+
+// Workspace of maxsim_rerank_two_stage: stage-1 scores and forward scratch,
+// candidate ids / stage-1 values / gathered offsets, the gather buffer (one
+// slice of k_candidates * max_doc_len rows per query), stage-2 scores and the
+// stage-2 forward's scratch (one query at a time).
+struct RerankLayout {
+    size_t s1 = 0, fwd8 = 0, cand = 0, cand_val = 0, cand_cu = 0, gather = 0, s2 = 0, fwd16 = 0, total = 0;
+    int64_t slice_rows = 0;
+};
+
+RerankLayout rerank_layout(int32_t n_q, int32_t lq_max, int32_t n_docs, int32_t k_cand, int32_t max_doc_len,
+                           maxsim_dtype_t dtype16) {
+    RerankLayout l;
+    l.slice_rows = static_cast<int64_t>(k_cand) * max_doc_len;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += align_up(bytes);
+        return at;
+    };
+    l.s1 = take(static_cast<size_t>(n_q) * n_docs * sizeof(float));
+    l.fwd8 = take(forward_layout(n_q, lq_max, n_docs, MAXSIM_INT8).total);
+    l.cand = take(static_cast<size_t>(n_q) * k_cand * sizeof(int32_t));
+    l.cand_val = take(static_cast<size_t>(n_q) * k_cand * sizeof(float));
+    l.cand_cu = take(static_cast<size_t>(n_q) * (k_cand + 1) * sizeof(int32_t));
+    l.gather = take(static_cast<size_t>(n_q) * l.slice_rows * kDim * 2);
+    l.s2 = take(static_cast<size_t>(n_q) * k_cand * sizeof(float));
+    l.fwd16 = take(forward_layout(1, lq_max, k_cand, dtype16).total);
+    l.total = off;
+    return l;
 }
 
 }  // namespace
@@ -365,6 +403,29 @@ maxsim_status_t maxsim_forward(const void *Q, const int32_t *q_lens, int32_t n_q
     if (st != MAXSIM_OK) return st;
     return forward_block(plan, D, cu_seqlens, n_docs, total_d_tokens, scores, raw_scores, argmax, n_docs,
                          stream);
+}
+
+maxsim_status_t maxsim_forward_int8_per_token(const int8_t *Q, const float *q_scales, const int32_t *q_lens,
+                                              int32_t n_q, int32_t lq_max, const int8_t *D, const float *d_scales,
+                                              const int32_t *cu_seqlens, int32_t n_docs, int64_t total_d_tokens,
+                                              int32_t dim, float *scores, int32_t *argmax, void *workspace,
+                                              size_t workspace_bytes, void *stream_) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    maxsim_status_t st = check_forward_args(Q, q_lens, n_q, lq_max, n_docs, total_d_tokens, dim, MAXSIM_INT8,
+                                            1.0f, 1.0f);
+    if (st != MAXSIM_OK) return st;
+    if (n_q == 0 || n_docs == 0) return MAXSIM_OK;
+    if (!cu_seqlens || !scores || (lq_max > 0 && !q_scales)) return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (total_d_tokens > 0 && (!D || !aligned16(D) || !d_scales)) return MAXSIM_ERR_INVALID_ARGUMENT;
+    const FwdLayout wl = forward_layout(n_q, lq_max, n_docs, MAXSIM_INT8);
+    if (wl.total > 0 && (workspace == nullptr || workspace_bytes < wl.total)) return MAXSIM_ERR_WORKSPACE;
+    ForwardPlan plan;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    st = forward_prepare(plan, Q, q_lens, n_q, lq_max, MAXSIM_INT8, 1.0f, 1.0f, ws, ws + wl.partials, stream,
+                         q_scales);
+    if (st != MAXSIM_OK) return st;
+    return forward_block(plan, D, cu_seqlens, n_docs, total_d_tokens, scores, nullptr, argmax, n_docs, stream,
+                         d_scales);
 }
 
 size_t maxsim_forward_host_workspace_size(int32_t n_q, int32_t lq_max, int32_t n_docs, int32_t block_docs,
@@ -455,6 +516,103 @@ maxsim_status_t maxsim_forward_host(const void *Q, const int32_t *q_lens, int32_
             return MAXSIM_ERR_CUDA;
     }
     return MAXSIM_OK;
+}
+
+maxsim_status_t maxsim_topk(const float *values, int32_t n_rows, int32_t n_cols, int64_t ld, int32_t k,
+                            int32_t *out_ids, float *out_values, void *stream_) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (n_rows < 0 || n_cols < 0 || k < 0 || ld < n_cols) return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (k > kTopkMax) return MAXSIM_ERR_UNSUPPORTED;
+    if (n_rows == 0 || k == 0) return MAXSIM_OK;
+    if (!out_ids || !out_values || (n_cols > 0 && !values)) return MAXSIM_ERR_INVALID_ARGUMENT;
+    return cuda_status(launch_topk(values, ld, n_rows, n_cols, k, nullptr, 0, out_ids, out_values, stream));
+}
+
+size_t maxsim_rerank_workspace_size(int32_t n_q, int32_t lq_max, int32_t n_docs, int32_t k_candidates,
+                                    int32_t max_doc_len, int32_t dim, maxsim_dtype_t dtype16) {
+    (void)dim;
+    if (n_q < 0 || lq_max < 0 || n_docs < 0 || k_candidates <= 0 || max_doc_len < 0) return 0;
+    return rerank_layout(n_q, lq_max, n_docs, k_candidates, max_doc_len, dtype16).total;
+}
+
+maxsim_status_t maxsim_rerank_two_stage(const int8_t *Q8, const float *q_tok_scales, float q_scale,
+                                        const int8_t *D8, const float *d_tok_scales, float d_scale,
+                                        const void *Q16, const void *D16, maxsim_dtype_t dtype16,
+                                        const int32_t *q_lens, int32_t n_q, int32_t lq_max,
+                                        const int32_t *cu_seqlens, int32_t n_docs, int64_t total_d_tokens,
+                                        int32_t max_doc_len, int32_t dim, int32_t k_candidates, int32_t k,
+                                        int32_t *top_ids, float *top_scores, int32_t *candidate_ids,
+                                        void *workspace, size_t workspace_bytes, void *stream_) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (dtype16 != MAXSIM_FP16 && dtype16 != MAXSIM_BF16) return MAXSIM_ERR_UNSUPPORTED;
+    const bool per_token = q_tok_scales != nullptr || d_tok_scales != nullptr;
+    if (per_token && (q_tok_scales == nullptr || (total_d_tokens > 0 && d_tok_scales == nullptr)))
+        return MAXSIM_ERR_INVALID_ARGUMENT;
+    maxsim_status_t st = check_forward_args(Q8, q_lens, n_q, lq_max, n_docs, total_d_tokens, dim, MAXSIM_INT8,
+                                            per_token ? 1.0f : q_scale, per_token ? 1.0f : d_scale);
+    if (st != MAXSIM_OK) return st;
+    if (k_candidates <= 0 || k < 0 || k > k_candidates || max_doc_len < 0) return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (k_candidates > kTopkMax) return MAXSIM_ERR_UNSUPPORTED;
+    if (n_q == 0) return MAXSIM_OK;
+    if (!cu_seqlens || !top_ids || !top_scores) return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (lq_max > 0 && (!Q16 || !aligned16(Q16))) return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (total_d_tokens > 0 && (!D8 || !aligned16(D8) || !D16 || !aligned16(D16)))
+        return MAXSIM_ERR_INVALID_ARGUMENT;
+    const RerankLayout l = rerank_layout(n_q, lq_max, n_docs, k_candidates, max_doc_len, dtype16);
+    if (l.slice_rows > INT32_MAX - 256) return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (workspace == nullptr || workspace_bytes < l.total) return MAXSIM_ERR_WORKSPACE;
+
+    // The FP16/BF16 corpus is read only by the gather: device memory, or
+    // page-locked host memory through its device mapping (zero-copy).
+    const void *d16 = D16;
+    if (total_d_tokens > 0) {
+        cudaPointerAttributes attr;
+        if (cudaPointerGetAttributes(&attr, D16) != cudaSuccess) return MAXSIM_ERR_INVALID_ARGUMENT;
+        if (attr.type == cudaMemoryTypeUnregistered || attr.devicePointer == nullptr)
+            return MAXSIM_ERR_INVALID_ARGUMENT;
+        d16 = attr.devicePointer;
+    }
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *s1 = reinterpret_cast<float *>(ws + l.s1);
+    int32_t *cand = candidate_ids ? candidate_ids : reinterpret_cast<int32_t *>(ws + l.cand);
+    float *cand_val = reinterpret_cast<float *>(ws + l.cand_val);
+    int32_t *cand_cu = reinterpret_cast<int32_t *>(ws + l.cand_cu);
+    uint8_t *gather = ws + l.gather;
+    float *s2 = reinterpret_cast<float *>(ws + l.s2);
+
+    // stage 1: every document, INT8
+    ForwardPlan p8;
+    const FwdLayout f8 = forward_layout(n_q, lq_max, n_docs, MAXSIM_INT8);
+    st = forward_prepare(p8, Q8, q_lens, n_q, lq_max, MAXSIM_INT8, q_scale, d_scale, ws + l.fwd8,
+                         ws + l.fwd8 + f8.partials, stream, per_token ? q_tok_scales : nullptr);
+    if (st != MAXSIM_OK) return st;
+    st = forward_block(p8, D8, cu_seqlens, n_docs, total_d_tokens, s1, nullptr, nullptr, n_docs, stream,
+                       per_token ? d_tok_scales : nullptr);
+    if (st != MAXSIM_OK) return st;
+    cudaError_t e = launch_topk(s1, n_docs, n_q, n_docs, k_candidates, nullptr, 0, cand, cand_val, stream);
+    if (e != cudaSuccess) return MAXSIM_ERR_CUDA;
+
+    // stage 2: each query's candidates, gathered and rescored in FP16/BF16
+    e = launch_candidate_offsets(cand, n_q, k_candidates, cu_seqlens, max_doc_len, cand_cu, p8.p.status, stream);
+    if (e == cudaSuccess && total_d_tokens > 0)
+        e = launch_gather_candidates(cand, n_q, k_candidates, cu_seqlens, cand_cu, d16, kDim * 2, gather,
+                                     l.slice_rows, p8.sm_count, stream);
+    if (e != cudaSuccess) return MAXSIM_ERR_CUDA;
+    const size_t q_stride = static_cast<size_t>(lq_max) * kDim * 2;
+    for (int32_t q = 0; q < n_q; ++q) {
+        ForwardPlan p16;
+        st = forward_prepare(p16, static_cast<const uint8_t *>(Q16) + q * q_stride, q_lens + q, 1, lq_max,
+                             dtype16, 1.0f, 1.0f, ws + l.fwd16, ws + l.fwd16, stream);
+        if (st != MAXSIM_OK) return st;
+        st = forward_block(p16, gather + static_cast<size_t>(q) * l.slice_rows * kDim * 2,
+                           cand_cu + static_cast<int64_t>(q) * (k_candidates + 1), k_candidates,
+                           std::max<int64_t>(l.slice_rows, 1), s2 + static_cast<int64_t>(q) * k_candidates,
+                           nullptr, nullptr, k_candidates, stream);
+        if (st != MAXSIM_OK) return st;
+    }
+    return cuda_status(launch_topk(s2, k_candidates, n_q, k_candidates, k, cand, k_candidates, top_ids, top_scores,
+                                   stream));
 }
 
 size_t maxsim_backward_workspace_size(int32_t n_q, int32_t lq_max, int32_t n_docs, int64_t total_d_tokens) {

@@ -2,7 +2,7 @@
 
 This module only *draws* inputs: document lengths, token embeddings
 (N(0,1) in fp32, L2-normalised per token, then rounded to the storage type),
-and symmetric per-tensor INT8 quantisation.  It holds none of the MaxSim
+and symmetric INT8 quantisation with one scale per tensor or per token.  It holds none of the MaxSim
 arithmetic, so both the CUDA path and the CPU oracle can consume its output.
 
 Recipe (the same for every workload; see ``WORKLOADS``):
@@ -114,6 +114,28 @@ def unit_tokens_int8(n_rows: int, dim: int, seed: int, device="cpu"):
         x = _unit_rows(e - s, dim, gen, device)
         out[s:e] = torch.clamp(torch.round(x / scale), -127, 127).to(torch.int8)
     return out, float(scale.item())
+
+
+def unit_tokens_int8_per_token(n_rows: int, dim: int, seed: int, device="cpu", with_fp16: bool = False):
+    """[n_rows, dim] unit-norm rows (the same seeded stream as unit_tokens)
+    quantised to INT8 with one symmetric scale per row: s = max|x| / 127 in
+    FP32, code = clamp(round-half-even(x / s), -127, 127).  Returns (int8
+    codes, float32 scales [n_rows]) and, with ``with_fp16``, the FP16 rows
+    the codes came from."""
+    gen = torch.Generator(device=device).manual_seed(seed)
+    codes = torch.empty((n_rows, dim), dtype=torch.int8, device=device)
+    scales = torch.empty((n_rows,), dtype=torch.float32, device=device)
+    f16 = torch.empty((n_rows, dim), dtype=torch.float16, device=device) if with_fp16 else None
+    for s in range(0, n_rows, _CHUNK_ROWS):
+        e = min(n_rows, s + _CHUNK_ROWS)
+        x = _unit_rows(e - s, dim, gen, device)
+        sc = (x.abs().amax(dim=1) / 127.0).to(torch.float32)
+        safe = torch.where(sc > 0, sc, torch.ones_like(sc))
+        codes[s:e] = torch.clamp(torch.round(x / safe[:, None]), -127, 127).to(torch.int8)
+        scales[s:e] = sc
+        if with_fp16:
+            f16[s:e] = x.to(torch.float16)
+    return (codes, scales, f16) if with_fp16 else (codes, scales)
 
 
 def make_inputs(w: Workload, device="cpu", n_docs: int | None = None, n_q: int | None = None):

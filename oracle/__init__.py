@@ -23,8 +23,8 @@ import numpy as np
 from ._build import build_oracle, library_path
 
 __all__ = [
-    "decode", "forward_bits", "forward_f64", "forward_i8", "dot_bits",
-    "backward_f64", "build_csr", "DTYPE_CODES",
+    "decode", "forward_bits", "forward_f64", "forward_i8", "forward_i8_token", "dot_bits",
+    "backward_f64", "build_csr", "topk", "rerank_two_stage", "DTYPE_CODES",
 ]
 
 DTYPE_CODES = {"fp16": 0, "bf16": 1}
@@ -63,6 +63,9 @@ def _load():
     lib.oracle_forward_i8.argtypes = [_i8p, _i32p, I32, I32, _i8p, _i32p, I32, I32, F32, F32,
                                       I64, _vp, _vp, _vp, _vp, _vp]
     lib.oracle_forward_i8.restype = INT
+    lib.oracle_forward_i8_token.argtypes = [_i8p, _f32p, _i32p, I32, I32, _i8p, _f32p, _i32p, I32, I32,
+                                            I64, _vp, _vp, _vp, _vp, _vp]
+    lib.oracle_forward_i8_token.restype = INT
     lib.oracle_backward_f64.argtypes = [_f64p, _i32p, _f64p, _i32p, I32, I32, _f64p, _i32p,
                                         I32, I32, _f64p, _f64p]
     lib.oracle_backward_f64.restype = INT
@@ -232,6 +235,98 @@ def forward_i8(Q, q_lens, D, cu_seqlens, q_scale, d_scale, pairs=None, threads=1
 
     _run_chunks(P, threads, run)
     return {"raw": raw, "score": score, "argmax": argmax}
+
+
+def forward_i8_token(Q, q_scales, q_lens, D, d_scales, cu_seqlens, pairs=None, want_rowmax=False,
+                     threads=1):
+    """Flash-MaxSim §4.3.1 INT8 x INT8 MaxSim with one scale per token (the
+    reading in oracle.c, R6): the value ranked is fp32(dot * d_scale[t]),
+    the row maximum is multiplied by the query token's scale and summed in
+    binary64.  Q int8 [n_q, lq_max, dim], q_scales f32 [n_q, lq_max], D int8
+    [total, dim], d_scales f32 [total].  Returns dict(score [P] f64, argmax
+    [P, lq_max] i32, and rowmax [P, lq_max] f32 when want_rowmax)."""
+    lib = _load()
+    Q = _c(Q, np.int8)
+    D = _c(D, np.int8)
+    qs = _c(q_scales, np.float32)
+    ds = _c(d_scales, np.float32)
+    q_lens = _c(q_lens, np.int32)
+    cu = _c(cu_seqlens, np.int32)
+    n_q, lq_max, dim = Q.shape
+    n_docs = cu.shape[0] - 1
+    pq, pb = _pairs(pairs, n_q, n_docs)
+    P = pq.shape[0]
+    score = np.empty(P, np.float64)
+    argmax = np.empty((P, lq_max), np.int32)
+    rowmax = np.empty((P, lq_max), np.float32) if want_rowmax else None
+    Dflat = D.reshape(-1) if D.size else np.zeros(1, np.int8)
+    dsflat = ds.reshape(-1) if ds.size else np.zeros(1, np.float32)
+
+    def run(s, e):
+        if e <= s:
+            return
+        rc = lib.oracle_forward_i8_token(Q.reshape(-1), qs.reshape(-1), q_lens, n_q, lq_max, Dflat, dsflat,
+                                         cu, n_docs, dim, e - s, _ptr(pq[s:e]), _ptr(pb[s:e]),
+                                         _ptr(score[s:e]), _ptr(argmax[s:e]),
+                                         _ptr(None if rowmax is None else rowmax[s:e]))
+        if rc != 0:
+            raise ValueError(f"oracle_forward_i8_token failed ({rc})")
+
+    _run_chunks(P, threads, run)
+    out = {"score": score, "argmax": argmax}
+    if want_rowmax:
+        out["rowmax"] = rowmax
+    return out
+
+
+def topk(values, k, ids=None):
+    """Per row of ``values`` [n_rows, n], the k largest entries in descending
+    order, ties to the lower column (a stable sort on the negated values).
+    Rows with fewer than k columns are padded with id -1 and value -inf.
+    ``ids`` [n_rows, n] maps a column to the id reported (default: the
+    column).  Returns (ids [n_rows, k] int32, values [n_rows, k])."""
+    values = np.asarray(values)
+    n_rows, n = values.shape
+    out_ids = np.full((n_rows, k), -1, np.int32)
+    out_val = np.full((n_rows, k), -np.inf, values.dtype)
+    m = min(k, n)
+    for r in range(n_rows):
+        order = np.argsort(-values[r], kind="stable")[:m]
+        out_ids[r, :m] = order if ids is None else np.asarray(ids)[r, order]
+        out_val[r, :m] = values[r, order]
+    return out_ids, out_val
+
+
+def rerank_two_stage(Q8, D8, q_scale, d_scale, dtype16, Q16_bits, D16_bits, q_lens, cu_seqlens, k_candidates,
+                     k, q_tok_scales=None, d_tok_scales=None, threads=1):
+    """The two-stage INT8 -> FP16 top-K scan of Flash-MaxSim §4.1 ("Kernel
+    Family"), read plainly: score every document with the INT8 MaxSim (one
+    scale per tensor, or per token when both token-scale arrays are given),
+    keep each query's k_candidates best documents (ties to the lower
+    document index), rescore those with the FP16/BF16 MaxSim and return each
+    query's k best of them.  Returns dict(cand_ids [n_q, k_candidates],
+    stage1 [n_q, n_docs], ids [n_q, k], scores [n_q, k] (binary64))."""
+    q_lens = _c(q_lens, np.int32)
+    cu = _c(cu_seqlens, np.int32)
+    n_q = q_lens.shape[0]
+    n_docs = cu.shape[0] - 1
+    if q_tok_scales is not None:
+        s1 = forward_i8_token(Q8, q_tok_scales, q_lens, D8, d_tok_scales, cu, threads=threads)["score"]
+    else:
+        s1 = forward_i8(Q8, q_lens, D8, cu, q_scale, d_scale, threads=threads)["score"]
+    s1 = s1.reshape(n_q, n_docs)
+    cand, _ = topk(s1, k_candidates)
+    pairs = np.array([(q, b) for q in range(n_q) for b in cand[q] if b >= 0], np.int32).reshape(-1, 2)
+    s2 = np.full((n_q, k_candidates), -np.inf)
+    if len(pairs):
+        sc = forward_bits(dtype16, Q16_bits, q_lens, D16_bits, cu, pairs=pairs, threads=threads)["score"]
+        pos = 0
+        for q in range(n_q):
+            m = int((cand[q] >= 0).sum())
+            s2[q, :m] = sc[pos:pos + m]
+            pos += m
+    ids, scores = topk(s2, k, ids=cand)
+    return {"cand_ids": cand, "stage1": s1, "ids": ids, "scores": scores}
 
 
 def backward_f64(grad, argmax, Q, q_lens, D, cu_seqlens):

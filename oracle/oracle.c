@@ -25,6 +25,14 @@
  *   R5  INT8 uses one symmetric scale per tensor (s_Q for Q, s_D for D); the
  *       score is fp32(raw * (s_Q * s_D)) evaluated in binary64 once at the
  *       end, where raw is the exact int64 sum of int32 row maxima.
+ *   R6  INT8 with one scale per token (the per-token quantisation of
+ *       Flash-MaxSim §4.3.1): the value ranked for query token i and document
+ *       token t is the single-precision product fp32(dot * s_D[t]) of the
+ *       exact integer dot product (below 2^24, so exact in binary32) and the
+ *       document token's scale; the row maximum and its lowest index are
+ *       taken on those values (the decision is made in binary32, the
+ *       precision the kernel ranks in), the query token's scale multiplies
+ *       the maximum, and the sum over query tokens runs in binary64.
  *
  * Parity status: every function here is pinned by CPU tests against closed
  * forms, invariants, brute force and finite differences (tests/test_oracle_*).
@@ -300,6 +308,61 @@ int oracle_forward_i8(const int8_t *Q, const int32_t *q_lens, int32_t n_q, int32
             raw[p] = sum;
             score[p] = (float)((double)sum * scale);
         }
+    }
+    return 0;
+}
+
+/*
+ * INT8 with one symmetric scale per token (R6).  q_scales [n_q, lq_max],
+ * d_scales [total]; outputs per pair: score (binary64; -inf for an empty
+ * document and a query with tokens), argmax [.., lq_max] and, when rowmax is
+ * non-NULL, the binary32 row maxima [.., lq_max] (-inf for padding / empty).
+ */
+int oracle_forward_i8_token(const int8_t *Q, const float *q_scales, const int32_t *q_lens, int32_t n_q,
+                            int32_t lq_max, const int8_t *D, const float *d_scales,
+                            const int32_t *cu_seqlens, int32_t n_docs, int32_t dim,
+                            int64_t n_pairs, const int32_t *pair_q, const int32_t *pair_b,
+                            double *score, int32_t *argmax, float *rowmax)
+{
+    if (n_q < 0 || n_docs < 0 || lq_max < 0 || dim <= 0) return -1;
+    if (pair_q == NULL) n_pairs = (int64_t)n_q * n_docs;
+    for (int64_t p = 0; p < n_pairs; ++p) {
+        int32_t q = pair_q ? pair_q[p] : (int32_t)(p / (n_docs ? n_docs : 1));
+        int32_t b = pair_q ? pair_b[p] : (int32_t)(p % (n_docs ? n_docs : 1));
+        if (q < 0 || q >= n_q || b < 0 || b >= n_docs) return -1;
+        int32_t lq = q_lens[q];
+        if (lq < 0 || lq > lq_max) return -1;
+        int64_t t0 = cu_seqlens[b];
+        int64_t ld = (int64_t)cu_seqlens[b + 1] - t0;
+        double sum = 0.0;
+        int empty = 0;
+        for (int32_t i = 0; i < lq_max; ++i) {
+            if (i >= lq) {
+                if (argmax) argmax[p * lq_max + i] = -1;
+                if (rowmax) rowmax[p * lq_max + i] = -INFINITY;
+                continue;
+            }
+            const int8_t *qi = Q + ((int64_t)q * lq_max + i) * dim;
+            float best = -INFINITY;
+            int64_t arg = -1;
+            for (int64_t t = 0; t < ld; ++t) {
+                const int8_t *dt = D + (t0 + t) * dim;
+                int64_t v = 0;
+                for (int k = 0; k < dim; ++k) v += (int64_t)qi[k] * (int64_t)dt[k];
+                if (v > 16777216 || v < -16777216) return -3;  /* exact in binary32 */
+                float dot = (float)v;
+                float scaled = dot * d_scales[t0 + t];          /* one binary32 rounding */
+                if (arg < 0 || scaled > best) {                  /* lowest t on ties */
+                    best = scaled;
+                    arg = t;
+                }
+            }
+            if (arg < 0) empty = 1;
+            else sum += (double)q_scales[(int64_t)q * lq_max + i] * (double)best;
+            if (argmax) argmax[p * lq_max + i] = (int32_t)arg;
+            if (rowmax) rowmax[p * lq_max + i] = best;
+        }
+        score[p] = empty ? -INFINITY : sum;
     }
     return 0;
 }

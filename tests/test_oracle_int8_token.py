@@ -1,0 +1,130 @@
+"""Pins for the oracle's INT8 forward with one scale per token (Flash-MaxSim
+§4.3.1, per-token symmetric quantisation; the reading: rank fp32(dot *
+s_D[t]), multiply the row maximum by s_Q[i], sum in binary64).  CPU only.
+
+  * unit scales reduce it to the per-tensor INT8 forward with scale 1, whose
+    raw integer sums are exact;
+  * power-of-two scales make every binary32 product exact, so an independent
+    float64 numpy brute force must agree bit for bit;
+  * for arbitrary scales the selected token's exact (real-number) value lies
+    within one binary32 rounding of the exact maximum;
+  * a planted mistake (the query scale dropped) fails the brute force."""
+import numpy as np
+
+import oracle
+
+RNG = np.random.default_rng(2024)
+
+
+def _cu(lengths):
+    return np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+
+
+def _case(n_q=3, lq=12, lengths=(5, 33, 1, 0, 17, 64), seed=0):
+    rng = np.random.default_rng(seed)
+    cu = _cu(np.array(lengths))
+    Q = rng.integers(-127, 128, (n_q, lq, 128)).astype(np.int8)
+    D = rng.integers(-127, 128, (int(cu[-1]), 128)).astype(np.int8)
+    q_lens = np.array([lq] + [max(0, lq - 5 * k) for k in range(1, n_q)], np.int32)
+    return Q, q_lens, D, cu
+
+
+def _brute_exact(Q, q_lens, D, cu, qs, ds):
+    """float64 brute force: exact when every product below is exact."""
+    n_q, lq = Q.shape[:2]
+    n_docs = len(cu) - 1
+    score = np.zeros((n_q, n_docs))
+    arg = -np.ones((n_q, n_docs, lq), np.int32)
+    for q in range(n_q):
+        for b in range(n_docs):
+            S = Q[q, :q_lens[q]].astype(np.float64) @ D[cu[b]:cu[b + 1]].astype(np.float64).T
+            S = S * ds[cu[b]:cu[b + 1]].astype(np.float64)[None, :]
+            if S.shape[1] == 0:
+                score[q, b] = -np.inf if q_lens[q] else 0.0
+                continue
+            arg[q, b, :q_lens[q]] = S.argmax(1)
+            score[q, b] = (S.max(1) * qs[q, :q_lens[q]].astype(np.float64)).sum()
+    return score, arg
+
+
+def test_unit_scales_equal_the_per_tensor_forward():
+    Q, q_lens, D, cu = _case()
+    qs = np.ones(Q.shape[:2], np.float32)
+    ds = np.ones(D.shape[0], np.float32)
+    tok = oracle.forward_i8_token(Q, qs, q_lens, D, ds, cu)
+    ten = oracle.forward_i8(Q, q_lens, D, cu, 1.0, 1.0)
+    finite = ten["raw"] != np.iinfo(np.int64).min
+    assert np.array_equal(tok["score"][finite], ten["raw"][finite].astype(np.float64))
+    assert np.all(np.isneginf(tok["score"][~finite]))
+    assert np.array_equal(tok["argmax"], ten["argmax"])
+
+
+def test_power_of_two_scales_match_float64_brute_force_exactly():
+    Q, q_lens, D, cu = _case(seed=1)
+    qs = np.exp2(RNG.integers(-12, -4, Q.shape[:2])).astype(np.float32)
+    ds = np.exp2(RNG.integers(-12, -4, D.shape[0])).astype(np.float32)
+    out = oracle.forward_i8_token(Q, qs, q_lens, D, ds, cu)
+    score, arg = _brute_exact(Q, q_lens, D, cu, qs, ds)
+    assert np.array_equal(out["score"], score.reshape(-1))
+    assert np.array_equal(out["argmax"], arg.reshape(-1, Q.shape[1]))
+
+
+def test_dropping_the_query_scale_is_caught():
+    """The brute force above is sensitive to the query-token scale."""
+    Q, q_lens, D, cu = _case(seed=2)
+    qs = np.exp2(RNG.integers(-12, -4, Q.shape[:2])).astype(np.float32)
+    ds = np.exp2(RNG.integers(-12, -4, D.shape[0])).astype(np.float32)
+    out = oracle.forward_i8_token(Q, qs, q_lens, D, ds, cu)
+    wrong, _ = _brute_exact(Q, q_lens, D, cu, np.ones_like(qs), ds)
+    finite = np.isfinite(wrong.reshape(-1)) & (wrong.reshape(-1) != 0)
+    assert not np.array_equal(out["score"][finite], wrong.reshape(-1)[finite])
+
+
+def test_general_scales_select_a_maximum_within_one_rounding():
+    Q, q_lens, D, cu = _case(seed=3)
+    qs = RNG.uniform(1e-3, 1e-2, Q.shape[:2]).astype(np.float32)
+    ds = RNG.uniform(1e-3, 1e-2, D.shape[0]).astype(np.float32)
+    out = oracle.forward_i8_token(Q, qs, q_lens, D, ds, cu, want_rowmax=True)
+    n_q, lq = Q.shape[:2]
+    n_docs = len(cu) - 1
+    for q in range(n_q):
+        for b in range(n_docs):
+            p = q * n_docs + b
+            S = Q[q, :q_lens[q]].astype(np.float64) @ D[cu[b]:cu[b + 1]].astype(np.float64).T
+            S = S * ds[cu[b]:cu[b + 1]].astype(np.float64)[None, :]
+            if S.shape[1] == 0 or q_lens[q] == 0:
+                continue
+            a = out["argmax"][p, :q_lens[q]]
+            chosen = S[np.arange(q_lens[q]), a]
+            best = S.max(1)
+            # the rounding of the selected and of the true maximum: 2^-24 each
+            assert np.all(best - chosen <= 2.0 ** -23 * np.abs(best) + 1e-300)
+            # the row maxima are the binary32 products of the chosen tokens
+            assert np.array_equal(out["rowmax"][p, :q_lens[q]], chosen.astype(np.float32))
+            # the score is the binary64 sum of query scale x row maximum
+            ref = (qs[q, :q_lens[q]].astype(np.float64) * chosen.astype(np.float32).astype(np.float64)).sum()
+            assert abs(out["score"][p] - ref) <= 1e-12 * max(1.0, abs(ref))
+
+
+def test_empty_documents_and_empty_queries():
+    Q, q_lens, D, cu = _case(n_q=2, lq=4, lengths=(0, 3, 0), seed=4)
+    q_lens = np.array([4, 0], np.int32)
+    qs = np.full(Q.shape[:2], 0.5, np.float32)
+    ds = np.full(D.shape[0], 0.25, np.float32)
+    out = oracle.forward_i8_token(Q, qs, q_lens, D, ds, cu)
+    sc = out["score"].reshape(2, 3)
+    assert np.isneginf(sc[0, 0]) and np.isneginf(sc[0, 2]) and np.isfinite(sc[0, 1])
+    assert np.array_equal(sc[1], [0.0, 0.0, 0.0])
+    assert np.all(out["argmax"].reshape(2, 3, 4)[0, 0] == -1)
+    assert np.all(out["argmax"].reshape(2, 3, 4)[1] == -1)
+
+
+def test_zero_scale_token_ranks_as_zero():
+    """A document token quantised from an all-zero vector has scale 0: its
+    value is 0 for every query token."""
+    Q = np.full((1, 1, 128), 1, np.int8)
+    D = np.stack([np.full(128, -1, np.int8), np.full(128, 5, np.int8)])
+    cu = _cu(np.array([2]))
+    out = oracle.forward_i8_token(Q, np.ones((1, 1), np.float32), [1], D, np.array([1.0, 0.0], np.float32), cu)
+    # token 0: -128 * 1 = -128; token 1: 640 * 0 = 0 -> token 1 wins
+    assert out["argmax"][0, 0] == 1 and out["score"][0] == 0.0
