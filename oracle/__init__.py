@@ -24,7 +24,8 @@ from ._build import build_oracle, library_path
 
 __all__ = [
     "decode", "forward_bits", "forward_f64", "forward_i8", "forward_i8_token", "dot_bits",
-    "backward_f64", "build_csr", "topk", "rerank_two_stage", "DTYPE_CODES",
+    "backward_f64", "build_csr", "topk", "rerank_two_stage", "chamfer_nn", "chamfer_forward",
+    "chamfer_backward", "chamfer_csr", "DTYPE_CODES",
 ]
 
 DTYPE_CODES = {"fp16": 0, "bf16": 1}
@@ -66,6 +67,12 @@ def _load():
     lib.oracle_forward_i8_token.argtypes = [_i8p, _f32p, _i32p, I32, I32, _i8p, _f32p, _i32p, I32, I32,
                                             I64, _vp, _vp, _vp, _vp, _vp]
     lib.oracle_forward_i8_token.restype = INT
+    lib.oracle_chamfer_nn.argtypes = [_f32p, _i32p, _f32p, _i32p, I32, _f32p, _i32p]
+    lib.oracle_chamfer_nn.restype = INT
+    lib.oracle_chamfer_reduce.argtypes = [_f32p, _i32p, _f32p, _i32p, I32, _f64p]
+    lib.oracle_chamfer_reduce.restype = INT
+    lib.oracle_chamfer_backward.argtypes = [_f32p, _i32p, _f32p, _i32p, I32, _i32p, _i32p, _f64p, _f64p, _f64p]
+    lib.oracle_chamfer_backward.restype = INT
     lib.oracle_backward_f64.argtypes = [_f64p, _i32p, _f64p, _i32p, I32, I32, _f64p, _i32p,
                                         I32, I32, _f64p, _f64p]
     lib.oracle_backward_f64.restype = INT
@@ -327,6 +334,75 @@ def rerank_two_stage(Q8, D8, q_scale, d_scale, dtype16, Q16_bits, D16_bits, q_le
             pos += m
     ids, scores = topk(s2, k, ids=cand)
     return {"cand_ids": cand, "stage1": s1, "ids": ids, "scores": scores}
+
+
+def _pts(a):
+    a = _c(a, np.float32).reshape(-1, 3)
+    return a if a.size else np.zeros((1, 3), np.float32)
+
+
+def chamfer_nn(S, cu_s, T, cu_t):
+    """Nearest target of every source point (reading R7 in oracle.c): binary32
+    squared distances [total_s] and target indices local to the item [total_s]."""
+    lib = _load()
+    cu_s, cu_t = _c(cu_s, np.int32), _c(cu_t, np.int32)
+    n = int(cu_s[-1])
+    dist = np.empty(max(n, 1), np.float32)
+    arg = np.empty(max(n, 1), np.int32)
+    rc = lib.oracle_chamfer_nn(_pts(S).reshape(-1), cu_s, _pts(T).reshape(-1), cu_t, cu_s.shape[0] - 1, dist, arg)
+    if rc != 0:
+        raise ValueError("oracle_chamfer_nn failed")
+    return dist[:n], arg[:n]
+
+
+def chamfer_forward(P, cu_p, Q, cu_q):
+    """Chamfer distance of every item (Flash-MaxSim §4.2, "Generalization to
+    Chamfer Distance"): dict(cd [B] f64, dist_pq, arg_pq, dist_qp, arg_qp)."""
+    lib = _load()
+    cu_p, cu_q = _c(cu_p, np.int32), _c(cu_q, np.int32)
+    d_pq, a_pq = chamfer_nn(P, cu_p, Q, cu_q)
+    d_qp, a_qp = chamfer_nn(Q, cu_q, P, cu_p)
+    B = cu_p.shape[0] - 1
+    cd = np.empty(max(B, 1), np.float64)
+    lib.oracle_chamfer_reduce(np.ascontiguousarray(d_pq) if d_pq.size else np.zeros(1, np.float32), cu_p,
+                              np.ascontiguousarray(d_qp) if d_qp.size else np.zeros(1, np.float32), cu_q, B, cd)
+    return {"cd": cd[:B], "dist_pq": d_pq, "arg_pq": a_pq, "dist_qp": d_qp, "arg_qp": a_qp}
+
+
+def chamfer_backward(P, cu_p, Q, cu_q, arg_pq, arg_qp, grad):
+    """Gradient of sum_b grad[b] * cd[b] for given nearest-neighbour indices,
+    in binary64 scatter form.  Returns (dP [N, 3], dQ [M, 3]) float64."""
+    lib = _load()
+    cu_p, cu_q = _c(cu_p, np.int32), _c(cu_q, np.int32)
+    N, M = int(cu_p[-1]), int(cu_q[-1])
+    dP = np.zeros(max(3 * N, 1), np.float64)
+    dQ = np.zeros(max(3 * M, 1), np.float64)
+    a_pq = _c(arg_pq, np.int32) if N else np.zeros(1, np.int32)
+    a_qp = _c(arg_qp, np.int32) if M else np.zeros(1, np.int32)
+    rc = lib.oracle_chamfer_backward(_pts(P).reshape(-1), cu_p, _pts(Q).reshape(-1), cu_q, cu_p.shape[0] - 1,
+                                     a_pq, a_qp, _c(grad, np.float64), dP, dQ)
+    if rc != 0:
+        raise ValueError("oracle_chamfer_backward failed")
+    return dP[:3 * N].reshape(N, 3), dQ[:3 * M].reshape(M, 3)
+
+
+def chamfer_csr(arg, cu_src, cu_dst):
+    """Inverse of a nearest-neighbour map (Flash-MaxSim §4.2.2 applied to
+    Chamfer): source i of item b points at destination cu_dst[b] + arg[i];
+    row_ptr [total_dst + 1] = exclusive cumulative count per destination,
+    col_idx = sources ordered by destination, ascending source within one
+    (a stable argsort of the destinations).  Sources with arg -1 are left
+    out."""
+    arg = np.asarray(arg, np.int64)
+    cu_src, cu_dst = np.asarray(cu_src, np.int64), np.asarray(cu_dst, np.int64)
+    item = np.repeat(np.arange(len(cu_src) - 1), np.diff(cu_src))
+    keep = arg >= 0
+    dst = cu_dst[item[keep]] + arg[keep]
+    src = np.nonzero(keep)[0]
+    order = np.argsort(dst, kind="stable")
+    row_ptr = np.zeros(int(cu_dst[-1]) + 1, np.int64)
+    np.add.at(row_ptr, dst + 1, 1)
+    return np.cumsum(row_ptr).astype(np.int32), src[order].astype(np.int32)
 
 
 def backward_f64(grad, argmax, Q, q_lens, D, cu_seqlens):

@@ -33,6 +33,15 @@
  *       taken on those values (the decision is made in binary32, the
  *       precision the kernel ranks in), the query token's scale multiplies
  *       the maximum, and the sum over query tokens runs in binary64.
+ *   R7  Chamfer distance (Flash-MaxSim §4.2 "Generalization to Chamfer
+ *       Distance"): the squared distance ranked for a source point s and a
+ *       target point t is the binary32 value
+ *           fma(dz, dz, fma(dy, dy, dx * dx)),  dx = s.x - t.x  (each step
+ *       rounded to nearest even), the precision and order the kernel ranks
+ *       in; the nearest target is the lowest index attaining the minimum; an
+ *       empty target set gives +inf and index -1.  The means over points and
+ *       the gradients are evaluated in binary64.  A mean over an empty set is
+ *       0.
  *
  * Parity status: every function here is pinned by CPU tests against closed
  * forms, invariants, brute force and finite differences (tests/test_oracle_*).
@@ -363,6 +372,100 @@ int oracle_forward_i8_token(const int8_t *Q, const float *q_scales, const int32_
             if (rowmax) rowmax[p * lq_max + i] = best;
         }
         score[p] = empty ? -INFINITY : sum;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Chamfer distance (R7).  Point sets are packed: item b owns source points  */
+/* cu_s[b] .. cu_s[b+1]-1 and target points cu_t[b] .. cu_t[b+1]-1, each a   */
+/* row of three binary32 coordinates.                                        */
+/* ------------------------------------------------------------------------- */
+
+static float chamfer_d2(const float *s, const float *t)
+{
+    float dx = s[0] - t[0];
+    float dy = s[1] - t[1];
+    float dz = s[2] - t[2];
+    float xx = dx * dx;
+    return fmaf(dz, dz, fmaf(dy, dy, xx));
+}
+
+/* Nearest target of every source point: dist [total_s] (binary32), arg
+ * [total_s] (index local to the item's target set, -1 when it is empty). */
+int oracle_chamfer_nn(const float *S, const int32_t *cu_s, const float *T, const int32_t *cu_t,
+                      int32_t n_items, float *dist, int32_t *arg)
+{
+    if (n_items < 0) return -1;
+    for (int32_t b = 0; b < n_items; ++b) {
+        int64_t t0 = cu_t[b], m = (int64_t)cu_t[b + 1] - t0;
+        for (int64_t s = cu_s[b]; s < cu_s[b + 1]; ++s) {
+            float best = INFINITY;
+            int64_t a = -1;
+            for (int64_t t = 0; t < m; ++t) {
+                float d = chamfer_d2(S + 3 * s, T + 3 * (t0 + t));
+                if (a < 0 || d < best) {     /* strict after the first: lowest t on ties */
+                    best = d;
+                    a = t;
+                }
+            }
+            dist[s] = best;
+            arg[s] = (int32_t)a;
+        }
+    }
+    return 0;
+}
+
+/* cd[b] = mean over P of its nearest-target distance + mean over Q of its
+ * nearest-source distance, from the binary32 distances, in binary64. */
+int oracle_chamfer_reduce(const float *dist_pq, const int32_t *cu_p, const float *dist_qp, const int32_t *cu_q,
+                          int32_t n_items, double *cd)
+{
+    for (int32_t b = 0; b < n_items; ++b) {
+        double a = 0.0, c = 0.0;
+        int64_t n = (int64_t)cu_p[b + 1] - cu_p[b], m = (int64_t)cu_q[b + 1] - cu_q[b];
+        for (int64_t i = cu_p[b]; i < cu_p[b + 1]; ++i) a += (double)dist_pq[i];
+        for (int64_t j = cu_q[b]; j < cu_q[b + 1]; ++j) c += (double)dist_qp[j];
+        cd[b] = (n ? a / (double)n : 0.0) + (m ? c / (double)m : 0.0);
+    }
+    return 0;
+}
+
+/* Gradient of sum_b grad[b] * cd[b] for the given nearest-neighbour indices,
+ * scattered straight from the chain rule in binary64: the term of point p
+ * with nearest target q contributes 2 g (p - q) / N to dP[p] and its negative
+ * to dQ[q] (and symmetrically for the Q -> P term with 1 / M). */
+int oracle_chamfer_backward(const float *P, const int32_t *cu_p, const float *Q, const int32_t *cu_q,
+                            int32_t n_items, const int32_t *arg_pq, const int32_t *arg_qp,
+                            const double *grad, double *dP, double *dQ)
+{
+    memset(dP, 0, sizeof(double) * 3 * (size_t)cu_p[n_items]);
+    memset(dQ, 0, sizeof(double) * 3 * (size_t)cu_q[n_items]);
+    for (int32_t b = 0; b < n_items; ++b) {
+        int64_t p0 = cu_p[b], n = (int64_t)cu_p[b + 1] - p0;
+        int64_t q0 = cu_q[b], m = (int64_t)cu_q[b + 1] - q0;
+        for (int64_t i = 0; i < n; ++i) {
+            int32_t a = arg_pq[p0 + i];
+            if (a < 0) continue;
+            if (a >= m) return -2;
+            double w = 2.0 * grad[b] / (double)n;
+            for (int k = 0; k < 3; ++k) {
+                double diff = (double)P[3 * (p0 + i) + k] - (double)Q[3 * (q0 + a) + k];
+                dP[3 * (p0 + i) + k] += w * diff;
+                dQ[3 * (q0 + a) + k] -= w * diff;
+            }
+        }
+        for (int64_t j = 0; j < m; ++j) {
+            int32_t a = arg_qp[q0 + j];
+            if (a < 0) continue;
+            if (a >= n) return -2;
+            double w = 2.0 * grad[b] / (double)m;
+            for (int k = 0; k < 3; ++k) {
+                double diff = (double)Q[3 * (q0 + j) + k] - (double)P[3 * (p0 + a) + k];
+                dQ[3 * (q0 + j) + k] += w * diff;
+                dP[3 * (p0 + a) + k] -= w * diff;
+            }
+        }
     }
     return 0;
 }

@@ -1,0 +1,166 @@
+"""Pins for the oracle's Chamfer distance (Flash-MaxSim §4.2 "Generalization
+to Chamfer Distance": the MaxSim skeleton with a min over squared Euclidean
+distances, and the backward through the inverse of the saved argmin).  CPU
+only.
+
+  * integer coordinates make every binary32 distance exact, so a float64
+    numpy brute force (np.argmin keeps the first minimum) must agree bit for
+    bit;
+  * P = Q gives distance 0 and the identity map; CD is symmetric and
+    invariant under an exact translation;
+  * for general points the selected neighbour lies within one binary32
+    rounding of the true minimum;
+  * the backward equals central finite differences of the float64 Chamfer
+    distance (piecewise quadratic: exact while no neighbour changes), obeys
+    the degree-2 homogeneity identity, and a sign error in it is caught;
+  * the CSR is a stable argsort of the destinations."""
+import numpy as np
+import pytest
+
+import oracle
+
+RNG = np.random.default_rng(31)
+
+
+def _brute(P, cu_p, Q, cu_q):
+    """float64 brute force: nearest neighbours both ways and the CD."""
+    d_pq, a_pq, d_qp, a_qp, cd = [], [], [], [], []
+    for b in range(len(cu_p) - 1):
+        Pb, Qb = P[cu_p[b]:cu_p[b + 1]].astype(np.float64), Q[cu_q[b]:cu_q[b + 1]].astype(np.float64)
+        D = ((Pb[:, None, :] - Qb[None, :, :]) ** 2).sum(-1)
+        if Qb.shape[0]:
+            a_pq += list(D.argmin(1)); d_pq += list(D.min(1))
+        else:
+            a_pq += [-1] * Pb.shape[0]; d_pq += [np.inf] * Pb.shape[0]
+        if Pb.shape[0]:
+            a_qp += list(D.argmin(0)); d_qp += list(D.min(0))
+        else:
+            a_qp += [-1] * Qb.shape[0]; d_qp += [np.inf] * Qb.shape[0]
+        t1 = D.min(1).mean() if D.size else 0.0
+        t2 = D.min(0).mean() if D.size else 0.0
+        cd.append((t1 if Pb.shape[0] else 0.0) + (t2 if Qb.shape[0] else 0.0))
+    return (np.array(d_pq), np.array(a_pq), np.array(d_qp), np.array(a_qp), np.array(cd))
+
+
+def _cu(sizes):
+    return np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+
+
+def test_integer_coordinates_match_brute_force_exactly():
+    cu_p, cu_q = _cu([17, 1, 40]), _cu([9, 30, 2])
+    P = RNG.integers(-20, 21, (int(cu_p[-1]), 3)).astype(np.float32)
+    Q = RNG.integers(-20, 21, (int(cu_q[-1]), 3)).astype(np.float32)
+    out = oracle.chamfer_forward(P, cu_p, Q, cu_q)
+    d_pq, a_pq, d_qp, a_qp, cd = _brute(P, cu_p, Q, cu_q)
+    assert np.array_equal(out["dist_pq"], d_pq.astype(np.float32))
+    assert np.array_equal(out["arg_pq"], a_pq)
+    assert np.array_equal(out["dist_qp"], d_qp.astype(np.float32))
+    assert np.array_equal(out["arg_qp"], a_qp)
+    assert np.allclose(out["cd"], cd, rtol=1e-15, atol=0)
+
+
+def test_identical_sets_symmetry_translation():
+    P = RNG.normal(size=(50, 3)).astype(np.float32)
+    cu = _cu([50])
+    out = oracle.chamfer_forward(P, cu, P, cu)
+    assert np.all(out["dist_pq"] == 0) and np.array_equal(out["arg_pq"], np.arange(50))
+    assert out["cd"][0] == 0.0
+    Q = RNG.normal(size=(70, 3)).astype(np.float32)
+    cq = _cu([70])
+    a = oracle.chamfer_forward(P, cu, Q, cq)["cd"]
+    b = oracle.chamfer_forward(Q, cq, P, cu)["cd"]
+    assert a[0] == b[0]
+    Pi = RNG.integers(-50, 50, (30, 3)).astype(np.float32)
+    Qi = RNG.integers(-50, 50, (40, 3)).astype(np.float32)
+    shift = np.array([7, -3, 11], np.float32)
+    c0 = oracle.chamfer_forward(Pi, _cu([30]), Qi, _cu([40]))
+    c1 = oracle.chamfer_forward(Pi + shift, _cu([30]), Qi + shift, _cu([40]))
+    assert c0["cd"][0] == c1["cd"][0] and np.array_equal(c0["arg_pq"], c1["arg_pq"])
+
+
+def test_ties_lowest_index_and_empty_sets():
+    P = np.zeros((1, 3), np.float32)
+    Q = np.array([[1, 0, 0], [0, 1, 0], [0, 0, -1], [2, 0, 0]], np.float32)
+    out = oracle.chamfer_forward(P, _cu([1]), Q, _cu([4]))
+    assert out["arg_pq"][0] == 0 and out["dist_pq"][0] == 1.0
+    assert list(out["arg_qp"]) == [0, 0, 0, 0]
+    out = oracle.chamfer_forward(P, _cu([1, 0]), Q, _cu([0, 4]))
+    assert out["arg_pq"][0] == -1 and np.isinf(out["dist_pq"][0])
+    assert np.all(out["arg_qp"] == -1) and np.isposinf(out["cd"][0])
+
+
+def test_general_points_within_one_rounding():
+    cu_p, cu_q = _cu([300]), _cu([200])
+    P = RNG.uniform(-1, 1, (300, 3)).astype(np.float32)
+    Q = RNG.uniform(-1, 1, (200, 3)).astype(np.float32)
+    out = oracle.chamfer_forward(P, cu_p, Q, cu_q)
+    D = ((P[:, None, :].astype(np.float64) - Q[None, :, :].astype(np.float64)) ** 2).sum(-1)
+    chosen = D[np.arange(300), out["arg_pq"]]
+    assert np.all(chosen - D.min(1) <= 2.0 ** -21 * D.min(1) + 2.0 ** -40)
+    assert np.allclose(out["dist_pq"], chosen, rtol=2.0 ** -20, atol=2.0 ** -40)
+
+
+def _cd64(P, cu_p, Q, cu_q, g):
+    return float(np.dot(g, _brute(P, cu_p, Q, cu_q)[4]))
+
+
+def _tie_free(n, m, seed):
+    rng = np.random.default_rng(seed)
+    while True:
+        P = rng.uniform(-1, 1, (n, 3))
+        Q = rng.uniform(-1, 1, (m, 3))
+        D = ((P[:, None] - Q[None]) ** 2).sum(-1)
+        s = np.sort(D, 1)
+        t = np.sort(D, 0)
+        if (s[:, 1] - s[:, 0]).min() > 1e-3 and (t[1] - t[0]).min() > 1e-3:
+            return P, Q
+
+
+def test_backward_equals_central_differences():
+    P, Q = _tie_free(12, 9, 5)
+    cu_p, cu_q = _cu([12]), _cu([9])
+    g = np.array([1.7])
+    fw = oracle.chamfer_forward(P.astype(np.float32), cu_p, Q.astype(np.float32), cu_q)
+    # the float64 coordinates are the float32 ones, so the function is exact
+    P, Q = P.astype(np.float32).astype(np.float64), Q.astype(np.float32).astype(np.float64)
+    dP, dQ = oracle.chamfer_backward(P.astype(np.float32), cu_p, Q.astype(np.float32), cu_q,
+                                     fw["arg_pq"], fw["arg_qp"], g)
+    h = 1e-5
+    for X, dX in ((P, dP), (Q, dQ)):
+        for i in range(X.shape[0]):
+            for k in range(3):
+                Xp, Xm = X.copy(), X.copy()
+                Xp[i, k] += h
+                Xm[i, k] -= h
+                if X is P:
+                    fp, fm = _cd64(Xp, cu_p, Q, cu_q, g), _cd64(Xm, cu_p, Q, cu_q, g)
+                else:
+                    fp, fm = _cd64(P, cu_p, Xp, cu_q, g), _cd64(P, cu_p, Xm, cu_q, g)
+                assert abs((fp - fm) / (2 * h) - dX[i, k]) <= 1e-8
+
+
+def test_backward_homogeneity_and_planted_sign_error():
+    """CD(cP, cQ) = c^2 CD(P, Q)  =>  <dP, P> + <dQ, Q> = 2 g CD."""
+    P, Q = _tie_free(20, 15, 6)
+    P, Q = P.astype(np.float32), Q.astype(np.float32)
+    cu_p, cu_q = _cu([20]), _cu([15])
+    fw = oracle.chamfer_forward(P, cu_p, Q, cu_q)
+    g = np.array([0.75])
+    dP, dQ = oracle.chamfer_backward(P, cu_p, Q, cu_q, fw["arg_pq"], fw["arg_qp"], g)
+    lhs = (dP * P.astype(np.float64)).sum() + (dQ * Q.astype(np.float64)).sum()
+    cd = _brute(P, cu_p, Q, cu_q)[4][0]
+    assert abs(lhs - 2 * 0.75 * cd) <= 1e-12
+    # a flipped sign on one side breaks the identity
+    assert abs((dP * P).sum() - (dQ * Q).sum() - 2 * 0.75 * cd) > 1e-3
+
+
+def test_csr_is_a_stable_argsort():
+    cu_src, cu_dst = _cu([5, 0, 6]), _cu([3, 4, 2])
+    arg = np.array([2, 0, 2, 1, 2, 1, 1, 0, -1, 1, 1])
+    row_ptr, col = oracle.chamfer_csr(arg, cu_src, cu_dst)
+    # item 0 sources 0-4 -> dst 2,0,2,1,2; item 2 sources 5-10 -> dst 7+1,7,-,7+1,7+1 ...
+    dst = {0: 2, 1: 0, 2: 2, 3: 1, 4: 2, 5: 8, 6: 8, 7: 7, 9: 8, 10: 8}
+    expect = sorted(dst, key=lambda s: (dst[s], s))
+    assert list(col) == expect
+    counts = np.bincount([dst[s] for s in dst], minlength=9)
+    assert list(row_ptr) == [0] + list(np.cumsum(counts))
