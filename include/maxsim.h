@@ -332,6 +332,79 @@ maxsim_status_t maxsim_backward(const float *grad_scores, const int32_t *argmax,
                                 float *dQ, float *dD,
                                 void *workspace, size_t workspace_bytes, void *stream);
 
+/* ------------------------------------------------------------------------ */
+/* Chamfer distance: Flash-MaxSim §4.2 "Generalization to Chamfer Distance".  */
+/* The MaxSim skeleton with a minimum over squared Euclidean distances:       */
+/*   CD(P, Q) = 1/N sum_p min_q |p - q|^2 + 1/M sum_q min_p |q - p|^2         */
+/* for a batch of point-set pairs packed like documents: item b owns points  */
+/* cu_p[b] .. cu_p[b+1]-1 of P and cu_q[b] .. cu_q[b+1]-1 of Q, each point a */
+/* row of three FP32 coordinates ([total, 3] row-major, device).              */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of workspace maxsim_chamfer_forward needs (0: none). */
+size_t maxsim_chamfer_forward_workspace_size(int32_t n_items, int64_t total_p, int64_t total_q, int32_t max_p,
+                                             int32_t max_q);
+
+/*
+ * Forward: for every point its nearest neighbour in the item's other set,
+ * ranked on the FP32 value fma(dz, dz, fma(dy, dy, dx * dx)) with
+ * dx = p.x - q.x (each step rounded to nearest even), the lowest index on
+ * ties; an empty other set gives +inf and index -1.
+ *   max_p, max_q   the largest |P_b| and |Q_b| (size the launch; a larger set
+ *               sets the device status word, code 0x203).
+ *   cd          FP32 [n_items]: the two means of the FP32 distances, summed
+ *               in binary64 in a fixed order (a mean over an empty set is 0).
+ *   dist_pq, arg_pq   FP32 / int32 [total_p]: nearest distance and the
+ *               index of the nearest point of Q_b (local to the item).
+ *   dist_qp, arg_qp   the same for Q against P_b.
+ * Coordinates must be finite with finite squared differences.
+ */
+maxsim_status_t maxsim_chamfer_forward(const float *P, const int32_t *cu_p, const float *Q, const int32_t *cu_q,
+                                       int32_t n_items, int64_t total_p, int64_t total_q, int32_t max_p,
+                                       int32_t max_q, float *cd, float *dist_pq, int32_t *arg_pq,
+                                       float *dist_qp, int32_t *arg_qp,
+                                       void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of workspace maxsim_chamfer_build_csr needs. */
+size_t maxsim_chamfer_csr_workspace_size(int64_t total_src, int64_t total_dst);
+
+/*
+ * Inverse-grid CSR of a nearest-neighbour map (Flash-MaxSim §4.2.2 applied
+ * to Chamfer): source point i of item b (cu_src[b] <= i < cu_src[b+1])
+ * points at destination r = cu_dst[b] + arg[i]; sources with arg -1 are
+ * left out.
+ *   row_ptr  int32 [total_dst + 1]: sources with destination < r.
+ *   col_idx  int32 [total_src]: the first row_ptr[total_dst] entries are the
+ *            sources ordered by destination, ascending source index within
+ *            one (a stable argsort); the rest is scratch.
+ * Built with a stable LSD radix sort (8-bit digits), no floating point and
+ * no order-dependent atomics.  An arg outside [-1, |dst_b|) sets the status
+ * word (code 0x201) and the source is left out.
+ */
+maxsim_status_t maxsim_chamfer_build_csr(const int32_t *arg, const int32_t *cu_src, const int32_t *cu_dst,
+                                         int32_t n_items, int64_t total_src, int64_t total_dst,
+                                         int32_t *row_ptr, int32_t *col_idx,
+                                         void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of workspace maxsim_chamfer_backward needs. */
+size_t maxsim_chamfer_backward_workspace_size(int64_t total_p, int64_t total_q);
+
+/*
+ * Backward of sum_b grad_cd[b] * CD_b through the saved nearest-neighbour
+ * indices: both CSRs are built, then each point's gradient is written once
+ * by its owner (no atomics):
+ *   dP[p] = 2 g / N_b (p - Q[arg_pq[p]])  +  2 g / M_b  sum_{q : arg_qp[q] = p} (p - q)
+ * and symmetrically for dQ; FP32, own term first, then the CSR sources in
+ * ascending order.
+ *   grad_cd  FP32 [n_items];  dP [total_p, 3], dQ [total_q, 3] FP32,
+ *   written in full.
+ */
+maxsim_status_t maxsim_chamfer_backward(const float *grad_cd, const float *P, const int32_t *cu_p,
+                                        const float *Q, const int32_t *cu_q, int32_t n_items,
+                                        int64_t total_p, int64_t total_q,
+                                        const int32_t *arg_pq, const int32_t *arg_qp, float *dP, float *dQ,
+                                        void *workspace, size_t workspace_bytes, void *stream);
+
 /*
  * Synchronises `stream`, then reads the device status word of the current
  * device (0 = no fault); `*code` receives the raw word when non-NULL.

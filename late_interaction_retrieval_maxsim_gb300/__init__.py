@@ -17,6 +17,8 @@ Entry points (same names as the C ABI):
   maxsim_forward_int8_per_token -- INT8 forward with one scale per token
   maxsim_topk      -- row-wise top-K selection (ties to the lower column)
   maxsim_rerank_two_stage -- INT8 scan, top-K' candidates, FP16 rescoring
+  maxsim_chamfer_forward / maxsim_chamfer_backward / maxsim_chamfer_build_csr
+                   -- the Chamfer distance on the same skeleton
   maxsim_device_status, maxsim_forward_workspace_size,
   maxsim_backward_workspace_size, maxsim_abi_version
 """
@@ -30,7 +32,8 @@ __all__ = [
     "maxsim_device_status", "maxsim_forward_workspace_size", "maxsim_backward_workspace_size",
     "maxsim_abi_version", "maxsim_forward_noalloc", "maxsim_forward_host",
     "maxsim_forward_host_workspace_size", "maxsim_forward_int8_per_token", "maxsim_topk",
-    "maxsim_rerank_two_stage", "maxsim_rerank_workspace_size", "MaxSimError", "DTYPE_CODES",
+    "maxsim_rerank_two_stage", "maxsim_rerank_workspace_size", "maxsim_chamfer_forward",
+    "maxsim_chamfer_backward", "maxsim_chamfer_build_csr", "MaxSimError", "DTYPE_CODES",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -96,6 +99,18 @@ def load_library():
     lib.maxsim_rerank_two_stage.argtypes = [vp, vp, f32, vp, vp, f32, vp, vp, ctypes.c_int, vp, i32, i32, vp,
                                             i32, i64, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
     lib.maxsim_rerank_two_stage.restype = ctypes.c_int
+    lib.maxsim_chamfer_forward_workspace_size.argtypes = [i32, i64, i64, i32, i32]
+    lib.maxsim_chamfer_forward_workspace_size.restype = sz
+    lib.maxsim_chamfer_forward.argtypes = [vp, vp, vp, vp, i32, i64, i64, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.maxsim_chamfer_forward.restype = ctypes.c_int
+    lib.maxsim_chamfer_csr_workspace_size.argtypes = [i64, i64]
+    lib.maxsim_chamfer_csr_workspace_size.restype = sz
+    lib.maxsim_chamfer_build_csr.argtypes = [vp, vp, vp, i32, i64, i64, vp, vp, vp, sz, vp]
+    lib.maxsim_chamfer_build_csr.restype = ctypes.c_int
+    lib.maxsim_chamfer_backward_workspace_size.argtypes = [i64, i64]
+    lib.maxsim_chamfer_backward_workspace_size.restype = sz
+    lib.maxsim_chamfer_backward.argtypes = [vp, vp, vp, vp, vp, i32, i64, i64, vp, vp, vp, vp, vp, sz, vp]
+    lib.maxsim_chamfer_backward.restype = ctypes.c_int
     lib.maxsim_device_status.argtypes = [vp, i32, ctypes.POINTER(i32)]
     lib.maxsim_device_status.restype = ctypes.c_int
     _LIB = lib
@@ -411,6 +426,93 @@ def maxsim_rerank_two_stage(Q8, D8, Q16, D16, q_lens, cu_seqlens, *, k_candidate
             _ptr(workspace), workspace.numel(), _stream(stream))
     _check("maxsim_rerank_two_stage", st)
     return ids, scores, cand
+
+
+def _sets(P, cu_p, Q, cu_q):
+    torch = _torch()
+    _require(P, "P", torch.float32)
+    dev = P.device
+    _require(Q, "Q", torch.float32, dev)
+    _require(cu_p, "cu_p", torch.int32, dev)
+    _require(cu_q, "cu_q", torch.int32, dev)
+    if P.dim() != 2 or P.shape[1] != 3 or Q.dim() != 2 or Q.shape[1] != 3:
+        raise ValueError("P and Q must be [total, 3] float32")
+    if cu_p.numel() != cu_q.numel():
+        raise ValueError("cu_p and cu_q must describe the same number of items")
+    return dev
+
+
+def maxsim_chamfer_forward(P, cu_p, Q, cu_q, *, max_p: int = None, max_q: int = None, workspace=None,
+                           stream=None):
+    """C: ``maxsim_chamfer_forward`` -- Chamfer distance of each item of a
+    packed batch of point-set pairs.  Returns (cd [B] float32, dist_pq,
+    arg_pq, dist_qp, arg_qp)."""
+    torch = _torch()
+    lib = load_library()
+    dev = _sets(P, cu_p, Q, cu_q)
+    n_items = cu_p.numel() - 1
+    if max_p is None:
+        max_p = int((cu_p[1:] - cu_p[:-1]).max()) if n_items else 0
+    if max_q is None:
+        max_q = int((cu_q[1:] - cu_q[:-1]).max()) if n_items else 0
+    N, M = P.shape[0], Q.shape[0]
+    cd = torch.empty(n_items, dtype=torch.float32, device=dev)
+    d_pq = torch.empty(N, dtype=torch.float32, device=dev)
+    a_pq = torch.empty(N, dtype=torch.int32, device=dev)
+    d_qp = torch.empty(M, dtype=torch.float32, device=dev)
+    a_qp = torch.empty(M, dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        ws_bytes = int(lib.maxsim_chamfer_forward_workspace_size(n_items, N, M, max_p, max_q))
+        if ws_bytes and (workspace is None or workspace.numel() < ws_bytes):
+            workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        st = lib.maxsim_chamfer_forward(_ptr(P), _ptr(cu_p), _ptr(Q), _ptr(cu_q), n_items, N, M, max_p, max_q,
+                                        _ptr(cd), _ptr(d_pq), _ptr(a_pq), _ptr(d_qp), _ptr(a_qp), _ptr(workspace),
+                                        workspace.numel() if workspace is not None else 0, _stream(stream))
+    _check("maxsim_chamfer_forward", st)
+    return cd, d_pq, a_pq, d_qp, a_qp
+
+
+def maxsim_chamfer_build_csr(arg, cu_src, cu_dst, total_dst: int, *, workspace=None, stream=None):
+    """C: ``maxsim_chamfer_build_csr`` -- (row_ptr [total_dst + 1], col_idx
+    [n_sources]) of a nearest-neighbour map; col_idx[:row_ptr[-1]] is valid."""
+    torch = _torch()
+    lib = load_library()
+    _require(arg, "arg", torch.int32)
+    dev = arg.device
+    n_items = cu_src.numel() - 1
+    row_ptr = torch.empty(total_dst + 1, dtype=torch.int32, device=dev)
+    col = torch.empty(max(arg.numel(), 1), dtype=torch.int32, device=dev)
+    need = int(lib.maxsim_chamfer_csr_workspace_size(arg.numel(), total_dst))
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.maxsim_chamfer_build_csr(_ptr(arg), _ptr(cu_src), _ptr(cu_dst), n_items, arg.numel(), total_dst,
+                                          _ptr(row_ptr), _ptr(col), _ptr(workspace), workspace.numel(),
+                                          _stream(stream))
+    _check("maxsim_chamfer_build_csr", st)
+    return row_ptr, col[:arg.numel()]
+
+
+def maxsim_chamfer_backward(grad_cd, P, cu_p, Q, cu_q, arg_pq, arg_qp, *, workspace=None, stream=None):
+    """C: ``maxsim_chamfer_backward`` -- (dP [N, 3], dQ [M, 3]) float32 of
+    sum_b grad_cd[b] * CD_b through the saved nearest-neighbour indices."""
+    torch = _torch()
+    lib = load_library()
+    dev = _sets(P, cu_p, Q, cu_q)
+    _require(grad_cd, "grad_cd", torch.float32, dev)
+    n_items = cu_p.numel() - 1
+    N, M = P.shape[0], Q.shape[0]
+    dP = torch.empty((N, 3), dtype=torch.float32, device=dev)
+    dQ = torch.empty((M, 3), dtype=torch.float32, device=dev)
+    need = int(lib.maxsim_chamfer_backward_workspace_size(N, M))
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.maxsim_chamfer_backward(_ptr(grad_cd), _ptr(P), _ptr(cu_p), _ptr(Q), _ptr(cu_q), n_items, N, M,
+                                         _ptr(arg_pq), _ptr(arg_qp), _ptr(dP), _ptr(dQ), _ptr(workspace),
+                                         workspace.numel(), _stream(stream))
+    _check("maxsim_chamfer_backward", st)
+    return dP, dQ
 
 
 def maxsim_build_csr(argmax, q_lens, cu_seqlens, total_d_tokens: int, *, workspace=None, stream=None):

@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
-SOURCES = ["maxsim_api.cu", "fwd_tc.cu", "bwd.cu", "noalloc.cu", "topk.cu"]
+SOURCES = ["maxsim_api.cu", "fwd_tc.cu", "bwd.cu", "noalloc.cu", "topk.cu", "chamfer.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -61,6 +61,23 @@ cudaError_t launch_gather_candidates(const int32_t *cand, int32_t n_q, int32_t n
                                      const int32_t *cand_cu, const void *src, int64_t row_bytes, void *dst,
                                      int64_t slice_rows, int sm_count, cudaStream_t stream);
 
+// chamfer.cu
+int chamfer_slices(int32_t n_items, int32_t max_s, int32_t max_t, int sm_count);
+cudaError_t launch_chamfer_nn(const float *S, const int32_t *cu_s, const float *T, const int32_t *cu_t,
+                              int32_t n_items, int32_t max_s, int32_t max_t, int64_t total_s, int slices,
+                              float *dist, int32_t *arg, float *part_d, int32_t *part_a, int32_t *status,
+                              cudaStream_t stream);
+cudaError_t launch_chamfer_reduce(const float *dist_pq, const int32_t *cu_p, const float *dist_qp,
+                                  const int32_t *cu_q, int32_t n_items, float *cd, cudaStream_t stream);
+size_t chamfer_csr_scratch_bytes(int64_t total_src, int32_t total_dst);
+cudaError_t launch_chamfer_csr(const int32_t *arg, const int32_t *cu_src, const int32_t *cu_dst, int32_t n_items,
+                               int64_t total_src, int32_t total_dst, int32_t *row_ptr, int32_t *col_idx,
+                               void *scratch, int32_t *status, cudaStream_t stream);
+cudaError_t launch_chamfer_grad(const float *grad, const float *A, const int32_t *cu_a, const float *B,
+                                const int32_t *cu_b, int32_t n_items, const int32_t *arg_ab,
+                                const int32_t *row_ptr_ba, const int32_t *col_ba, int64_t total_a, float *dA,
+                                cudaStream_t stream);
+
 // bwd.cu
 struct BwdParams {
     const float *grad;       // [n_q, n_docs]

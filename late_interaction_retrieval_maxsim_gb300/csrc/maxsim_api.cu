@@ -353,6 +353,54 @@ RerankLayout rerank_layout(int32_t n_q, int32_t lq_max, int32_t n_docs, int32_t 
     return l;
 }
 
+maxsim_status_t check_chamfer_sets(int32_t n_items, int64_t total_p, int64_t total_q, int32_t max_p,
+                                   int32_t max_q) {
+    if (n_items < 0 || total_p < 0 || total_q < 0 || max_p < 0 || max_q < 0) return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (total_p > INT32_MAX - 1 || total_q > INT32_MAX - 1) return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (max_p > total_p || max_q > total_q) return MAXSIM_ERR_INVALID_ARGUMENT;
+    return MAXSIM_OK;
+}
+
+struct ChamferFwdLayout {
+    int slices_pq = 1, slices_qp = 1;
+    size_t part_d = 0, part_a = 0, total = 0;
+};
+
+ChamferFwdLayout chamfer_fwd_layout(int32_t n_items, int64_t total_p, int64_t total_q, int32_t max_p,
+                                    int32_t max_q, int sm_count) {
+    ChamferFwdLayout l;
+    l.slices_pq = chamfer_slices(n_items, max_p, max_q, sm_count);
+    l.slices_qp = chamfer_slices(n_items, max_q, max_p, sm_count);
+    const int64_t elems = std::max<int64_t>(l.slices_pq > 1 ? l.slices_pq * total_p : 0,
+                                            l.slices_qp > 1 ? l.slices_qp * total_q : 0);
+    l.part_d = 0;
+    l.part_a = align_up(static_cast<size_t>(elems) * sizeof(float));
+    l.total = l.part_a + align_up(static_cast<size_t>(elems) * sizeof(int32_t));
+    return l;
+}
+
+struct ChamferBwdLayout {
+    size_t row_qp = 0, col_qp = 0, row_pq = 0, col_pq = 0, scratch = 0, total = 0;
+};
+
+ChamferBwdLayout chamfer_bwd_layout(int64_t total_p, int64_t total_q) {
+    ChamferBwdLayout l;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += align_up(bytes);
+        return at;
+    };
+    l.row_qp = take(static_cast<size_t>(total_p + 1) * 4);
+    l.col_qp = take(static_cast<size_t>(std::max<int64_t>(total_q, 1)) * 4);
+    l.row_pq = take(static_cast<size_t>(total_q + 1) * 4);
+    l.col_pq = take(static_cast<size_t>(std::max<int64_t>(total_p, 1)) * 4);
+    l.scratch = take(std::max(chamfer_csr_scratch_bytes(total_q, static_cast<int32_t>(total_p)),
+                              chamfer_csr_scratch_bytes(total_p, static_cast<int32_t>(total_q))));
+    l.total = off;
+    return l;
+}
+
 }  // namespace
 }  // namespace maxsim
 
@@ -613,6 +661,103 @@ maxsim_status_t maxsim_rerank_two_stage(const int8_t *Q8, const float *q_tok_sca
     }
     return cuda_status(launch_topk(s2, k_candidates, n_q, k_candidates, k, cand, k_candidates, top_ids, top_scores,
                                    stream));
+}
+
+size_t maxsim_chamfer_forward_workspace_size(int32_t n_items, int64_t total_p, int64_t total_q, int32_t max_p,
+                                             int32_t max_q) {
+    if (check_chamfer_sets(n_items, total_p, total_q, max_p, max_q) != MAXSIM_OK) return 0;
+    DeviceInfo di;
+    if (device_info(&di) != MAXSIM_OK) return 0;
+    return chamfer_fwd_layout(n_items, total_p, total_q, max_p, max_q, di.sm_count).total;
+}
+
+maxsim_status_t maxsim_chamfer_forward(const float *P, const int32_t *cu_p, const float *Q, const int32_t *cu_q,
+                                       int32_t n_items, int64_t total_p, int64_t total_q, int32_t max_p,
+                                       int32_t max_q, float *cd, float *dist_pq, int32_t *arg_pq, float *dist_qp,
+                                       int32_t *arg_qp, void *workspace, size_t workspace_bytes, void *stream_) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    maxsim_status_t st = check_chamfer_sets(n_items, total_p, total_q, max_p, max_q);
+    if (st != MAXSIM_OK) return st;
+    if (n_items == 0) return MAXSIM_OK;
+    if (!cu_p || !cu_q || !cd || (total_p > 0 && (!P || !dist_pq || !arg_pq)) ||
+        (total_q > 0 && (!Q || !dist_qp || !arg_qp)))
+        return MAXSIM_ERR_INVALID_ARGUMENT;
+    DeviceInfo di;
+    if ((st = device_info(&di)) != MAXSIM_OK) return st;
+    const ChamferFwdLayout l = chamfer_fwd_layout(n_items, total_p, total_q, max_p, max_q, di.sm_count);
+    if (l.total > 0 && (workspace == nullptr || workspace_bytes < l.total)) return MAXSIM_ERR_WORKSPACE;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *part_d = reinterpret_cast<float *>(ws + l.part_d);
+    int32_t *part_a = reinterpret_cast<int32_t *>(ws + l.part_a);
+    cudaError_t e = launch_chamfer_nn(P, cu_p, Q, cu_q, n_items, max_p, max_q, total_p, l.slices_pq, dist_pq,
+                                      arg_pq, part_d, part_a, di.status, stream);
+    if (e == cudaSuccess)
+        e = launch_chamfer_nn(Q, cu_q, P, cu_p, n_items, max_q, max_p, total_q, l.slices_qp, dist_qp, arg_qp,
+                              part_d, part_a, di.status, stream);
+    if (e == cudaSuccess) e = launch_chamfer_reduce(dist_pq, cu_p, dist_qp, cu_q, n_items, cd, stream);
+    return cuda_status(e);
+}
+
+size_t maxsim_chamfer_csr_workspace_size(int64_t total_src, int64_t total_dst) {
+    if (total_src < 0 || total_dst < 0 || total_dst > INT32_MAX - 1) return 0;
+    return chamfer_csr_scratch_bytes(total_src, static_cast<int32_t>(total_dst));
+}
+
+maxsim_status_t maxsim_chamfer_build_csr(const int32_t *arg, const int32_t *cu_src, const int32_t *cu_dst,
+                                         int32_t n_items, int64_t total_src, int64_t total_dst, int32_t *row_ptr,
+                                         int32_t *col_idx, void *workspace, size_t workspace_bytes,
+                                         void *stream_) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (n_items < 0 || total_src < 0 || total_dst < 0 || total_src > INT32_MAX - 1 || total_dst > INT32_MAX - 1)
+        return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (n_items == 0 && (total_src > 0 || total_dst > 0)) return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (!row_ptr || (n_items > 0 && (!cu_src || !cu_dst)) || (total_src > 0 && (!arg || !col_idx)))
+        return MAXSIM_ERR_INVALID_ARGUMENT;
+    const size_t need = chamfer_csr_scratch_bytes(total_src, static_cast<int32_t>(total_dst));
+    if (workspace == nullptr || workspace_bytes < need) return MAXSIM_ERR_WORKSPACE;
+    DeviceInfo di;
+    maxsim_status_t st = device_info(&di);
+    if (st != MAXSIM_OK) return st;
+    return cuda_status(launch_chamfer_csr(arg, cu_src, cu_dst, n_items, total_src, static_cast<int32_t>(total_dst),
+                                          row_ptr, col_idx, workspace, di.status, stream));
+}
+
+size_t maxsim_chamfer_backward_workspace_size(int64_t total_p, int64_t total_q) {
+    if (total_p < 0 || total_q < 0 || total_p > INT32_MAX - 1 || total_q > INT32_MAX - 1) return 0;
+    return chamfer_bwd_layout(total_p, total_q).total;
+}
+
+maxsim_status_t maxsim_chamfer_backward(const float *grad_cd, const float *P, const int32_t *cu_p, const float *Q,
+                                        const int32_t *cu_q, int32_t n_items, int64_t total_p, int64_t total_q,
+                                        const int32_t *arg_pq, const int32_t *arg_qp, float *dP, float *dQ,
+                                        void *workspace, size_t workspace_bytes, void *stream_) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    maxsim_status_t st = check_chamfer_sets(n_items, total_p, total_q, 0, 0);
+    if (st != MAXSIM_OK) return st;
+    if (n_items == 0) return MAXSIM_OK;
+    if (!grad_cd || !cu_p || !cu_q || (total_p > 0 && (!P || !arg_pq || !dP)) ||
+        (total_q > 0 && (!Q || !arg_qp || !dQ)))
+        return MAXSIM_ERR_INVALID_ARGUMENT;
+    const ChamferBwdLayout l = chamfer_bwd_layout(total_p, total_q);
+    if (workspace == nullptr || workspace_bytes < l.total) return MAXSIM_ERR_WORKSPACE;
+    DeviceInfo di;
+    if ((st = device_info(&di)) != MAXSIM_OK) return st;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int32_t *row_qp = reinterpret_cast<int32_t *>(ws + l.row_qp);
+    int32_t *col_qp = reinterpret_cast<int32_t *>(ws + l.col_qp);
+    int32_t *row_pq = reinterpret_cast<int32_t *>(ws + l.row_pq);
+    int32_t *col_pq = reinterpret_cast<int32_t *>(ws + l.col_pq);
+    // inverse of Q -> P (destinations in P) and of P -> Q (destinations in Q)
+    cudaError_t e = launch_chamfer_csr(arg_qp, cu_q, cu_p, n_items, total_q, static_cast<int32_t>(total_p), row_qp,
+                                       col_qp, ws + l.scratch, di.status, stream);
+    if (e == cudaSuccess)
+        e = launch_chamfer_csr(arg_pq, cu_p, cu_q, n_items, total_p, static_cast<int32_t>(total_q), row_pq, col_pq,
+                               ws + l.scratch, di.status, stream);
+    if (e == cudaSuccess)
+        e = launch_chamfer_grad(grad_cd, P, cu_p, Q, cu_q, n_items, arg_pq, row_qp, col_qp, total_p, dP, stream);
+    if (e == cudaSuccess)
+        e = launch_chamfer_grad(grad_cd, Q, cu_q, P, cu_p, n_items, arg_qp, row_pq, col_pq, total_q, dQ, stream);
+    return cuda_status(e);
 }
 
 size_t maxsim_backward_workspace_size(int32_t n_q, int32_t lq_max, int32_t n_docs, int64_t total_d_tokens) {

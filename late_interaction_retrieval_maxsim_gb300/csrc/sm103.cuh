@@ -22,6 +22,7 @@ enum : int32_t {
     kStatusTimeoutDrain = 0x104,
     kStatusBadArgmax = 0x201,
     kStatusDocTooLong = 0x202,
+    kStatusSetTooLarge = 0x203,
 };
 
 // 2 s: far beyond any legitimate single wait in these kernels.
