@@ -21,8 +21,10 @@ Rank 0 prints ONE JSON line.  Besides the contract keys it carries:
   e2e           the same metric with host-resident inputs copied in and the
                 scores copied back every step,
   clocks        SM clocks sampled by nvidia-smi during the timed region,
-  extra         the other workloads (ColPali, training fwd+bwd, INT8, and
-                out-of-core scoring of a host-resident corpus).
+  extra         the other workloads (ColPali, training fwd+bwd, INT8 with one
+                scale per tensor and per token, the two-stage INT8 -> FP16
+                top-K scan, out-of-core scoring of a host-resident corpus,
+                and the Chamfer distance of two 100K-point clouds).
 
 ``--impl reference`` times the CPU oracle (the only reference this method
 has) on the same workload, metric and unit.
@@ -225,6 +227,7 @@ def _extra_workloads(m, syn, rl, peaks):
         del x, Q, D, s, a
         torch.cuda.empty_cache()
     out["out_of_core_colpali"] = _out_of_core(m, syn)
+    out.update(_int8_variants(m, syn))
     return out
 
 
@@ -271,6 +274,90 @@ def _out_of_core(m, syn, steps=3, n_docs=100_000, block_docs=20_000, ld=1024, lq
     if m.maxsim_device_status() != 0:
         rec["device_status"] = "fault"
     del D_h, cu_h, ws
+    torch.cuda.empty_cache()
+    return rec
+
+
+def _int8_variants(m, syn, steps=10):
+    """§4.3.1 per-token INT8 on the 32 x 32 vs 100,000-document varlen shape,
+    and the two-stage INT8 -> FP16 top-K scan (§4.1 "Kernel Family") on the
+    same corpus: INT8 scan of every document, 1,000 candidates per query
+    rescored in FP16, the best 100 returned."""
+    import torch
+    dev = torch.device("cuda")
+    stream = torch.cuda.current_stream()
+    w = syn.WORKLOADS["int8_varlen"]
+    cu = syn.cu_seqlens_from_lengths(syn.doc_lengths(w.n_docs, w.ld_lo, w.ld_hi, w.seed)).to(dev)
+    total = int(cu[-1])
+    ql = torch.full((w.n_q,), w.lq, dtype=torch.int32, device=dev)
+    out = {}
+    Q8, qs = syn.unit_tokens_int8_per_token(w.n_q * w.lq, w.dim, w.seed + 1, dev)
+    D8, ds = syn.unit_tokens_int8_per_token(total, w.dim, w.seed + 2, dev)
+    Q8, qs = Q8.view(w.n_q, w.lq, w.dim), qs.view(w.n_q, w.lq)
+    s, a = m.maxsim_forward_int8_per_token(Q8, qs, ql, D8, ds, cu)
+    _, per = _time_loop(lambda: m.maxsim_forward_int8_per_token(Q8, qs, ql, D8, ds, cu, scores=s, argmax=a),
+                        steps, 3, stream)
+    ms = statistics.median(per)
+    out["int8_per_token"] = {"n_q": w.n_q, "lq": w.lq, "n_docs": w.n_docs, "ld": [w.ld_lo, w.ld_hi],
+                             "fwd_ms": round(ms, 4), "docs_per_s": w.n_docs / (ms / 1e3)}
+    del Q8, D8, qs, ds, s, a
+    Q8, qst = syn.unit_tokens_int8(w.n_q * w.lq, w.dim, w.seed + 1, dev)
+    D8, dst = syn.unit_tokens_int8(total, w.dim, w.seed + 2, dev)
+    Q8 = Q8.view(w.n_q, w.lq, w.dim)
+    Q16 = syn.unit_tokens(w.n_q * w.lq, w.dim, w.seed + 1, "fp16", dev).view(w.n_q, w.lq, w.dim)
+    D16 = syn.unit_tokens(total, w.dim, w.seed + 2, "fp16", dev)
+    kc, k = 1000, 100
+    ws = torch.empty(m.maxsim_rerank_workspace_size(w.n_q, w.lq, w.n_docs, kc, w.ld_hi, "fp16"),
+                     dtype=torch.uint8, device=dev)
+
+    def rerank():
+        m.maxsim_rerank_two_stage(Q8, D8, Q16, D16, ql, cu, k_candidates=kc, k=k, q_scale=qst, d_scale=dst,
+                                  max_doc_len=w.ld_hi, workspace=ws)
+    _, per = _time_loop(rerank, steps, 3, stream)
+    ms = statistics.median(per)
+    out["rerank_two_stage"] = {"n_q": w.n_q, "lq": w.lq, "n_docs": w.n_docs, "k_candidates": kc, "k": k,
+                               "stage1": "int8 per tensor", "stage2": "fp16, corpus in HBM",
+                               "call_ms": round(ms, 4), "queries_per_s": w.n_q / (ms / 1e3)}
+    if m.maxsim_device_status() != 0:
+        out["device_status"] = "fault"
+    del Q8, D8, Q16, D16, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+CHAMFER_LANE_OPS_PER_PAIR = 7   # 3 sub, 1 mul, 2 fma, 1 min on the FP32 lanes
+
+
+def _chamfer(m, sm_max_mhz, n=100_000, steps=10):
+    """§4.2 "Generalization to Chamfer Distance" at the pages' 100K-point
+    scale: one pair of 100,000-point clouds (uniform in the unit cube),
+    forward (nearest neighbours both ways) and backward.  The search is
+    bound by FP32 lane throughput: the roofline counts 7 lane operations per
+    point pair against 128 FP32 lanes per SM at the maximum SM clock."""
+    import torch
+    dev = torch.device("cuda")
+    stream = torch.cuda.current_stream()
+    g = torch.Generator("cuda").manual_seed(0)
+    P = torch.rand((n, 3), generator=g, device=dev)
+    Q = torch.rand((n, 3), generator=g, device=dev)
+    cu = torch.tensor([0, n], dtype=torch.int32, device=dev)
+    fw = m.maxsim_chamfer_forward(P, cu, Q, cu)
+    _, per = _time_loop(lambda: m.maxsim_chamfer_forward(P, cu, Q, cu, max_p=n, max_q=n), steps, 3, stream)
+    ms = statistics.median(per)
+    gcd = torch.ones(1, device=dev)
+    _, perb = _time_loop(lambda: m.maxsim_chamfer_backward(gcd, P, cu, Q, cu, fw[2], fw[4]), steps, 3, stream)
+    msb = statistics.median(perb)
+    pairs = 2.0 * n * n
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    peak = sms * 128 * sm_max_mhz * 1e6 * 1e-12
+    achieved = pairs * CHAMFER_LANE_OPS_PER_PAIR / (ms / 1e3) * 1e-12
+    rec = {"points": [n, n], "fwd_ms": round(ms, 4), "bwd_ms": round(msb, 4), "pairs_per_s": pairs / (ms / 1e3),
+           "roofline": {"bound": "alu", "achieved": round(achieved, 2), "peak": round(peak, 2),
+                        "unit": "T FP32 lane-ops/s", "frac": round(achieved / peak, 3),
+                        "peak_source": f"{sms} SMs x 128 FP32 lanes x {sm_max_mhz:.0f} MHz"}}
+    if m.maxsim_device_status() != 0:
+        rec["device_status"] = "fault"
+    del P, Q
     torch.cuda.empty_cache()
     return rec
 
@@ -389,6 +476,7 @@ def run_ours(args):
     if rank == 0 and world == 1:
         if not args.no_extra:
             extra = _extra_workloads(m, syn, rl, peaks)
+            extra["chamfer_100k"] = _chamfer(m, clk.summary().get("sm_max_mhz") or 2070.0)
         cpu = _cpu_baseline(x, budget_s=args.cpu_budget)
     if world > 1:
         import torch.distributed as dist
