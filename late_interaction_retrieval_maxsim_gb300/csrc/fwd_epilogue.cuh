@@ -233,7 +233,7 @@ template <bool ARGMAX, bool INT8, bool SCALE, bool DB, typename SlotOf, typename
 __device__ __forceinline__ void epilogue_warp(const FwdParams &p, int rho_warp, int64_t rows_total,
                                               uint32_t tmem_base, int qd, int b_begin, int b_end,
                                               int t_begin, int t_end, int n_tiles, uint64_t *t_full,
-                                              SlotOf slot_of, Release release,
+                                              float *scale_slot, SlotOf slot_of, Release release,
                                               volatile int32_t *abort_flag, bool cluster_scope) {
     const int lane = threadIdx.x & 31;
     const bool warp_rows = rho_warp < rows_total;
@@ -248,14 +248,27 @@ __device__ __forceinline__ void epilogue_warp(const FwdParams &p, int rho_warp, 
 
     // SCALE: lane l holds the scale of column c0 + l of the next chunk (0
     // past this CTA's tokens); every column of the row is multiplied by its
-    // scale, broadcast by shuffles.
+    // scale.  The warp passes the scales through its 16-float shared slot,
+    // half a chunk at a time, and every lane reads them back as broadcasts.
     auto chunk_scale = [&](int c0) -> float {
         return (SCALE && c0 + lane < t_end) ? __ldg(p.d_tok_scale + c0 + lane) : 0.0f;
     };
     auto apply_scale = [&](uint32_t (&r)[32], float s) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k)
-            r[k] = __float_as_uint(__uint_as_float(r[k]) * __shfl_sync(0xffffffffu, s, k));
+        for (int h = 0; h < 2; ++h) {
+            __syncwarp();
+            if ((lane >> 4) == h) scale_slot[lane & 15] = s;
+            __syncwarp();
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+                const float4 v = reinterpret_cast<const float4 *>(scale_slot)[k4];
+                const int k = 16 * h + 4 * k4;
+                r[k] = __float_as_uint(__uint_as_float(r[k]) * v.x);
+                r[k + 1] = __float_as_uint(__uint_as_float(r[k + 1]) * v.y);
+                r[k + 2] = __float_as_uint(__uint_as_float(r[k + 2]) * v.z);
+                r[k + 3] = __float_as_uint(__uint_as_float(r[k + 3]) * v.w);
+            }
+        }
     };
 
     // Upcoming document boundaries: lane l holds cu[cu_base + l]; one

@@ -50,6 +50,8 @@ constexpr int kTmemCols = kSlots * kSlotCols;  // 512: the whole TMEM
 constexpr int kMaxStages = 4;
 
 struct SharedCtl {
+    // per-token INT8: one 16-column scale slot per epilogue warp (broadcast reads)
+    alignas(16) float scale_buf[16][16];
     uint64_t q_full;
     uint64_t d_full[kMaxStages];    // FP16 D stage ready for the MMA
     uint64_t d_empty[kMaxStages];   // FP16 D stage consumed by the MMA
@@ -273,7 +275,7 @@ maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         if (mt < n_mt) {
             epilogue_warp<ARGMAX, INT8 && !SCALE, SCALE, C::kDoubleBuffer>(
                 p, row0 + mt * 128 + qd * 32, rows_total, tmem_base, qd, b_begin, b_end, t_begin, t_end,
-                n_tiles, ctl->t_full,
+                n_tiles, ctl->t_full, ctl->scale_buf[warp - C::kFirstEpiWarp],
                 [&](int j) { return make_int2(mt + NMT * (j % (kSlots / NMT)), j / (kSlots / NMT)); },
                 [&](int slot) { mbar_arrive(&ctl->t_empty[slot]); }, abort_flag, false);
         }

@@ -57,6 +57,8 @@ WORKLOADS = {
                         note="1 query Lq=1024 vs 10,000 docs Ld=1024"),
     "train": Workload("train", 256, 32, 256, 180, 180, "bf16",
                       note="256 queries Lq=32 x 256 docs Ld=180, BF16, fwd+bwd"),
+    "train_colpali": Workload("train_colpali", 64, 1024, 64, 1024, 1024, "bf16",
+                              note="64 queries Lq=1024 x 64 docs Ld=1024, BF16, fwd+bwd"),
     "int8_varlen": Workload("int8_varlen", 32, 32, 100_000, 32, 512, "int8",
                             note="32 queries Lq=32 vs 100,000 docs Ld~U[32,512], INT8"),
 }

@@ -68,6 +68,18 @@ def test_ragged_with_empty_docs_and_padding(ops, dtype):
     assert torch.all(dQ[1] == 0) and torch.all(dQ[2, 17:] == 0)
 
 
+def test_long_queries_colpali_like(ops):
+    """Queries of hundreds of tokens against page-length documents (the
+    ColPali training shape of Flash-MaxSim §5 "Training Step", scaled down):
+    CSR bit-exact, dQ / dD within tolerance."""
+    lengths = [700, 1024, 3, 512, 1000, 257]
+    Q, ql, D, cu = random_case(6, 300, lengths, "bf16", [300, 1, 129, 257, 32, 300], seed=41)
+    scores, argmax, _ = ops.maxsim_forward(Q, ql, D, cu)
+    g = _contrastive_grad(scores)
+    _check_csr(ops, argmax, ql, cu, D.shape[0])
+    _check_backward(ops, g, argmax, Q, ql, D, cu, "bf16")
+
+
 def test_hot_tokens_skewed_argmax(ops):
     """A skewed winner map (half the rows pick token 0 of their document):
     the CSR keeps ascending source order inside each hot row."""
