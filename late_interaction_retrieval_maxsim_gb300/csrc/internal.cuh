@@ -91,10 +91,24 @@ struct BwdParams {
     int32_t *row_ptr;        // [total + 1]
     int32_t *col_idx;        // [n_q * n_docs * lq_max]
     int32_t *doc_count;      // [n_docs + 1] scratch: sources per document, then offsets
+    int32_t *chunk_cnt;      // [chunks * total] scratch: per-chunk token counts, then first slots
     int32_t *status;
     int32_t n_q, lq_max, n_docs, total_tokens;
+    int32_t chunks;          // candidate chunks per document (csr_chunks)
     int32_t bf16;
+    uint32_t lq_magic, lq_shift;  // k / lq_max == (k * lq_magic) >> (31 + lq_shift) for 0 <= k < 2^31
 };
+
+// Division by a fixed divisor d >= 1 for numerators below 2^31 (Granlund and
+// Montgomery, "Division by invariant integers using multiplication", 1994):
+// s = ceil(log2 d), m = ceil(2^(31+s) / d); then m * d - 2^(31+s) < d <= 2^s,
+// which makes floor(n * m / 2^(31+s)) == floor(n / d) for 0 <= n < 2^31.
+inline void make_divisor(int32_t d, uint32_t &m, uint32_t &s) {
+    s = 0;
+    while ((int64_t{1} << s) < d) ++s;
+    m = static_cast<uint32_t>(((uint64_t{1} << (31 + s)) + static_cast<uint64_t>(d) - 1) / static_cast<uint64_t>(d));
+}
+int csr_chunks(int32_t n_q, int32_t lq_max, int32_t n_docs);
 cudaError_t launch_build_csr(const BwdParams &p, cudaStream_t stream);
 cudaError_t launch_grad_d(const BwdParams &p, cudaStream_t stream);
 cudaError_t launch_grad_q(const BwdParams &p, cudaStream_t stream);

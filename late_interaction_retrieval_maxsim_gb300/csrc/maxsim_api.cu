@@ -134,7 +134,7 @@ FwdLayout forward_layout(int32_t n_q, int32_t lq_max, int32_t n_docs, maxsim_dty
 }
 
 struct BwdLayout {
-    size_t row_ptr = 0, col_idx = 0, doc_count = 0, total = 0;
+    size_t row_ptr = 0, col_idx = 0, doc_count = 0, chunk_cnt = 0, total = 0;
 };
 
 BwdLayout backward_layout(int32_t n_q, int32_t lq_max, int32_t n_docs, int64_t total) {
@@ -142,7 +142,8 @@ BwdLayout backward_layout(int32_t n_q, int32_t lq_max, int32_t n_docs, int64_t t
     l.row_ptr = align_up(static_cast<size_t>(total + 1) * 4);
     l.col_idx = align_up(static_cast<size_t>(std::max<int64_t>(1, int64_t(n_q) * n_docs * lq_max)) * 4);
     l.doc_count = align_up(static_cast<size_t>(n_docs + 1) * 4);
-    l.total = l.row_ptr + l.col_idx + l.doc_count;
+    l.chunk_cnt = align_up(static_cast<size_t>(csr_chunks(n_q, lq_max, n_docs)) * std::max<int64_t>(total, 1) * 4);
+    l.total = l.row_ptr + l.col_idx + l.doc_count + l.chunk_cnt;
     return l;
 }
 
@@ -790,6 +791,9 @@ static void fill_bwd_params(BwdParams &p, const int32_t *argmax, const int32_t *
     p.row_ptr = reinterpret_cast<int32_t *>(ws);
     p.col_idx = reinterpret_cast<int32_t *>(ws + l.row_ptr);
     p.doc_count = reinterpret_cast<int32_t *>(ws + l.row_ptr + l.col_idx);
+    p.chunk_cnt = reinterpret_cast<int32_t *>(ws + l.row_ptr + l.col_idx + l.doc_count);
+    p.chunks = csr_chunks(n_q, lq_max, n_docs);
+    make_divisor(std::max(1, lq_max), p.lq_magic, p.lq_shift);
     p.status = di.status;
 }
 

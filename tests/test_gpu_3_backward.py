@@ -80,6 +80,20 @@ def test_long_queries_colpali_like(ops):
     _check_backward(ops, g, argmax, Q, ql, D, cu, "bf16")
 
 
+def test_csr_documents_split_into_chunks(ops):
+    """16 queries x 1024 tokens: each document's 16,384 candidate sources are
+    split into several chunks placed by separate CTAs; the CSR must still be
+    the unique stable argsort (hot tokens make many sources share a row
+    across chunk borders)."""
+    lengths = [1024] * 10 + [3, 700, 1]
+    Q, ql, D, cu = random_case(16, 1024, lengths, "bf16", [1024] * 8 + [1000, 1, 0, 512] + [700] * 4, seed=43)
+    D[cu[0]:cu[0] + 4] = Q[0, :4]            # a few document tokens that many query tokens pick
+    _, argmax, _ = ops.maxsim_forward(Q, ql, D, cu)
+    _check_csr(ops, argmax, ql, cu, D.shape[0])
+    g = torch.randn((16, len(lengths)), device="cuda", generator=torch.Generator("cuda").manual_seed(4))
+    _check_backward(ops, g, argmax, Q, ql, D, cu, "bf16")
+
+
 def test_hot_tokens_skewed_argmax(ops):
     """A skewed winner map (half the rows pick token 0 of their document):
     the CSR keeps ascending source order inside each hot row."""
