@@ -426,10 +426,23 @@ int grid_of(int64_t n, int threads, int cap) {
 }  // namespace
 
 int chamfer_slices(int32_t n_items, int32_t max_s, int32_t max_t, int sm_count) {
-    const int64_t ctas = static_cast<int64_t>(n_items) * ((max_s + kNnSources - 1) / kNnSources);
-    const int64_t want = (4LL * sm_count + std::max<int64_t>(ctas, 1) - 1) / std::max<int64_t>(ctas, 1);
-    const int64_t cap = std::max<int64_t>(1, max_t / 2048);
-    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, std::min<int64_t>(cap, 64))));
+    // CTAs = items x source tiles x slices run in waves of `slots` (two per
+    // SM); a CTA's time is proportional to its slice, 1 / s of the targets,
+    // so the search takes ceil(ctas / slots) / s.  Take the smallest s within
+    // 5 % of the best (fewer, larger CTAs; each slice keeps at least 2,048
+    // targets, at most 64 slices).
+    const int64_t tiles = static_cast<int64_t>(n_items) * ((max_s + kNnSources - 1) / kNnSources);
+    const int64_t slots = 2LL * std::max(sm_count, 1);
+    const int64_t cap = std::max<int64_t>(1, std::min<int64_t>(64, max_t / 2048));
+    if (tiles <= 0) return 1;
+    auto cost = [&](int64_t sl) {
+        return static_cast<double>((tiles * sl + slots - 1) / slots) / static_cast<double>(sl);
+    };
+    double best = cost(1);
+    for (int64_t sl = 2; sl <= cap; ++sl) best = std::min(best, cost(sl));
+    for (int64_t sl = 1; sl <= cap; ++sl)
+        if (cost(sl) <= best * 1.05) return static_cast<int>(sl);
+    return 1;
 }
 
 cudaError_t launch_chamfer_nn(const float *S, const int32_t *cu_s, const float *T, const int32_t *cu_t,
