@@ -119,3 +119,13 @@ def test_host_corpus_argument_errors_return_before_touching_the_device(lib):
     assert call(cu, 2, 64, need, total=40) == 1        # cu[n_docs] != total
     assert call(cu, 2, 64, need - 1) == 3              # workspace too small
     assert lib.maxsim_forward_host_workspace_size(1, 32, 3, 0, 64, 128, 0) == 0
+
+
+def test_run_case_driver_parses_without_a_gpu():
+    """The profiling driver imports and parses its arguments on a machine
+    without a GPU (it touches the device only when a case runs)."""
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, "-m", "late_interaction_retrieval_maxsim_gb300.run_case", "--help"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and "chamfer" in r.stdout
