@@ -10,6 +10,8 @@ entry point ``--reps`` times, synchronises and checks the device status word.
     python -m late_interaction_retrieval_maxsim_gb300.run_case int8-token --n-docs 5000
     python -m late_interaction_retrieval_maxsim_gb300.run_case backward --workload train
     python -m late_interaction_retrieval_maxsim_gb300.run_case chamfer --points 20000
+    python -m late_interaction_retrieval_maxsim_gb300.run_case rerank --n-docs 20000
+    python -m late_interaction_retrieval_maxsim_gb300.run_case host --n-docs 20000
 """
 from __future__ import annotations
 
@@ -19,7 +21,7 @@ import sys
 import torch
 
 from . import (maxsim_backward, maxsim_chamfer_backward, maxsim_chamfer_forward, maxsim_device_status,
-               maxsim_forward, maxsim_forward_int8_per_token)
+               maxsim_forward, maxsim_forward_host, maxsim_forward_int8_per_token, maxsim_rerank_two_stage)
 from . import synthetic as syn
 
 
@@ -65,7 +67,37 @@ def _chamfer(a):
         maxsim_chamfer_backward(torch.ones(1, device="cuda"), P, cu, Q, cu, apq, aqp)
 
 
-CASES = {"forward": _forward, "int8-token": _int8_token, "backward": _backward, "chamfer": _chamfer}
+def _rerank(a):
+    """Two-stage scan on the INT8 varlen workload: 1,000 candidates, 100 kept."""
+    w = syn.WORKLOADS["int8_varlen"]
+    n_docs = a.n_docs or w.n_docs
+    cu = syn.cu_seqlens_from_lengths(syn.doc_lengths(w.n_docs, w.ld_lo, w.ld_hi, w.seed)[:n_docs]).cuda()
+    total = int(cu[-1])
+    Q8, qs = syn.unit_tokens_int8(w.n_q * w.lq, w.dim, w.seed + 1, "cuda")
+    D8, ds = syn.unit_tokens_int8(total, w.dim, w.seed + 2, "cuda")
+    Q16 = syn.unit_tokens(w.n_q * w.lq, w.dim, w.seed + 1, "fp16", "cuda").view(w.n_q, w.lq, w.dim)
+    D16 = syn.unit_tokens(total, w.dim, w.seed + 2, "fp16", "cuda")
+    ql = torch.full((w.n_q,), w.lq, dtype=torch.int32, device="cuda")
+    for _ in range(a.reps):
+        maxsim_rerank_two_stage(Q8.view(w.n_q, w.lq, w.dim), D8, Q16, D16, ql, cu, k_candidates=1000, k=100,
+                                q_scale=qs, d_scale=ds, max_doc_len=w.ld_hi)
+
+
+def _host(a):
+    """Out-of-core forward: the ColBERT workload's corpus in pinned host
+    memory, streamed in blocks of 5,000 documents."""
+    w = syn.WORKLOADS["colbert_varlen"]
+    x = syn.make_inputs(w, device="cuda", n_docs=a.n_docs)
+    D_h = x["D"].cpu().pin_memory()
+    cu_h = x["cu_seqlens"].cpu().pin_memory()
+    for _ in range(a.reps):
+        maxsim_forward_host(x["Q"], x["q_lens"], D_h, cu_h, block_docs=5000, block_tokens=5000 * w.ld_hi,
+                            with_argmax=True)
+    torch.cuda.synchronize()
+
+
+CASES = {"forward": _forward, "int8-token": _int8_token, "backward": _backward, "chamfer": _chamfer,
+         "rerank": _rerank, "host": _host}
 
 
 def main(argv=None) -> int:
