@@ -323,6 +323,7 @@ maxsim_status_t maxsim_build_csr(const int32_t *argmax, const int32_t *q_lens, i
  *   dQ          FP32 [n_q, lq_max, dim], written in full (padding rows 0).
  *   dD          FP32 [total_d_tokens, dim], written in full (rows nobody
  *               selected are 0).
+ *   Q, D, dQ and dD must start on a 16-byte boundary.
  * dtype: FP16 or BF16 (INT8 returns MAXSIM_ERR_UNSUPPORTED).
  */
 maxsim_status_t maxsim_backward(const float *grad_scores, const int32_t *argmax,

@@ -829,6 +829,10 @@ maxsim_status_t maxsim_backward(const float *grad_scores, const int32_t *argmax,
     if (st != MAXSIM_OK) return st;
     if ((n_q > 0 && lq_max > 0 && (!dQ || !Q)) || (total_d_tokens > 0 && (!dD || !D)))
         return MAXSIM_ERR_INVALID_ARGUMENT;
+    // rows are read with vector loads and gradient rows written with 16-byte stores
+    if ((n_q > 0 && lq_max > 0 && (!aligned16(Q) || !aligned16(dQ))) ||
+        (total_d_tokens > 0 && (!aligned16(D) || !aligned16(dD))))
+        return MAXSIM_ERR_INVALID_ARGUMENT;
     if (n_q > 0 && n_docs > 0 && !grad_scores) return MAXSIM_ERR_INVALID_ARGUMENT;
     const BwdLayout l = backward_layout(n_q, lq_max, n_docs, total_d_tokens);
     if (!workspace || workspace_bytes < l.total) return MAXSIM_ERR_WORKSPACE;

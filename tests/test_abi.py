@@ -129,3 +129,17 @@ def test_run_case_driver_parses_without_a_gpu():
     r = subprocess.run([sys.executable, "-m", "late_interaction_retrieval_maxsim_gb300.run_case", "--help"],
                        cwd=ROOT, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0 and "chamfer" in r.stdout
+
+
+def test_backward_rejects_misaligned_rows(lib):
+    """Rows are moved with vector loads and stores: a pointer off a 16-byte
+    boundary is an argument error, reported before any device work."""
+    vp = ctypes.c_void_p
+    b = lib.maxsim_backward
+    ws = 1 << 20
+    ok = [vp(256), vp(256), vp(256), vp(256), 1, 32, vp(256), vp(256), 1, 10, 128, 0,
+          vp(256), vp(256), vp(256), ws, None]
+    for pos in (2, 6, 12, 13):          # Q, D, dQ, dD
+        args = list(ok)
+        args[pos] = vp(256 + 8)
+        assert b(*args) == 1
