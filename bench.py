@@ -216,6 +216,18 @@ def _extra_workloads(m, syn, rl, peaks):
             _, perb = _time_loop(lambda: m.maxsim_backward(g, a, Q, ql, D, cu, dQ=dq, dD=dd,
                                                            workspace=bws), 20, 3, stream)
             msb = statistics.median(perb)
+
+            # the training pair: the forward counts the CSR's sources, the
+            # backward skips its histogram pass
+            def train_step():
+                m.maxsim_forward_with_counts(Q, ql, D, cu, scores=s, argmax=a, workspace=ws, backward_workspace=bws)
+                m.maxsim_backward_with_counts(g, a, Q, ql, D, cu, bws, dQ=dq, dD=dd)
+            _, pers = _time_loop(train_step, 20, 3, stream)
+            _, perf = _time_loop(lambda: m.maxsim_forward_with_counts(Q, ql, D, cu, scores=s, argmax=a, workspace=ws,
+                                                                      backward_workspace=bws), 20, 3, stream)
+            rec.update(train_step_ms=round(statistics.median(pers), 4),
+                       train_fwd_counting_ms=round(statistics.median(perf), 4),
+                       train_bwd_counted_ms=round(statistics.median(pers) - statistics.median(perf), 4))
             bb = rl.backward_hbm_bytes(w.n_q, w.lq, w.n_docs, D.shape[0], int(ql.sum()) * w.n_docs)
             n_src = int(ql.sum()) * w.n_docs
             rec.update(bwd_ms=round(msb, 4), step_ms=round(ms + msb, 4),

@@ -407,6 +407,38 @@ maxsim_status_t maxsim_chamfer_backward(const float *grad_cd, const float *P, co
                                         void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Training forward: maxsim_forward (FP16/BF16, argmax required) that also
+ * counts, in its epilogue, the sources of the backward's inverse-grid CSR.
+ * Flash-MaxSim §4.2.2 derives that CSR from the saved argmax during the
+ * training step; counting while the argmax is produced saves the backward
+ * one pass over it.  The counts go into `backward_workspace` (at least
+ * maxsim_backward_workspace_size() bytes), which must then be handed,
+ * unchanged, to maxsim_backward_with_counts together with this call's
+ * argmax.  `workspace` is the forward's own scratch, as for maxsim_forward.
+ * Scores and argmax are identical to maxsim_forward's.
+ */
+maxsim_status_t maxsim_forward_with_counts(const void *Q, const int32_t *q_lens, int32_t n_q, int32_t lq_max,
+                                           const void *D, const int32_t *cu_seqlens, int32_t n_docs,
+                                           int64_t total_d_tokens, int32_t dim, maxsim_dtype_t dtype,
+                                           float *scores, int32_t *argmax,
+                                           void *workspace, size_t workspace_bytes,
+                                           void *backward_workspace, size_t backward_workspace_bytes,
+                                           void *stream);
+
+/*
+ * maxsim_backward after maxsim_forward_with_counts: the same arguments and
+ * results, with `workspace` the forward's `backward_workspace` (its counts
+ * are used instead of a histogram pass over the argmax; the workspace is
+ * consumed -- a second backward needs a new counting forward).
+ */
+maxsim_status_t maxsim_backward_with_counts(const float *grad_scores, const int32_t *argmax,
+                                            const void *Q, const int32_t *q_lens, int32_t n_q, int32_t lq_max,
+                                            const void *D, const int32_t *cu_seqlens, int32_t n_docs,
+                                            int64_t total_d_tokens, int32_t dim, maxsim_dtype_t dtype,
+                                            float *dQ, float *dD,
+                                            void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Synchronises `stream`, then reads the device status word of the current
  * device (0 = no fault); `*code` receives the raw word when non-NULL.
  * When `clear` is non-zero the word is reset to 0.  Returns MAXSIM_OK,

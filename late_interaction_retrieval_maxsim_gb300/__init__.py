@@ -19,6 +19,9 @@ Entry points (same names as the C ABI):
   maxsim_rerank_two_stage -- INT8 scan, top-K' candidates, FP16 rescoring
   maxsim_chamfer_forward / maxsim_chamfer_backward / maxsim_chamfer_build_csr
                    -- the Chamfer distance on the same skeleton
+  maxsim_forward_with_counts / maxsim_backward_with_counts
+                   -- the training pair: the forward counts the backward's
+                      CSR sources while it produces the argmax
   maxsim_device_status, maxsim_forward_workspace_size,
   maxsim_backward_workspace_size, maxsim_abi_version
 """
@@ -33,7 +36,8 @@ __all__ = [
     "maxsim_abi_version", "maxsim_forward_noalloc", "maxsim_forward_host",
     "maxsim_forward_host_workspace_size", "maxsim_forward_int8_per_token", "maxsim_topk",
     "maxsim_rerank_two_stage", "maxsim_rerank_workspace_size", "maxsim_chamfer_forward",
-    "maxsim_chamfer_backward", "maxsim_chamfer_build_csr", "MaxSimError", "DTYPE_CODES",
+    "maxsim_chamfer_backward", "maxsim_chamfer_build_csr", "maxsim_forward_with_counts",
+    "maxsim_backward_with_counts", "MaxSimError", "DTYPE_CODES",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -111,6 +115,11 @@ def load_library():
     lib.maxsim_chamfer_backward_workspace_size.restype = sz
     lib.maxsim_chamfer_backward.argtypes = [vp, vp, vp, vp, vp, i32, i64, i64, vp, vp, vp, vp, vp, sz, vp]
     lib.maxsim_chamfer_backward.restype = ctypes.c_int
+    lib.maxsim_forward_with_counts.argtypes = [vp, vp, i32, i32, vp, vp, i32, i64, i32, ctypes.c_int, vp, vp,
+                                               vp, sz, vp, sz, vp]
+    lib.maxsim_forward_with_counts.restype = ctypes.c_int
+    lib.maxsim_backward_with_counts.argtypes = lib.maxsim_backward.argtypes
+    lib.maxsim_backward_with_counts.restype = ctypes.c_int
     lib.maxsim_device_status.argtypes = [vp, i32, ctypes.POINTER(i32)]
     lib.maxsim_device_status.restype = ctypes.c_int
     _LIB = lib
@@ -568,6 +577,67 @@ def maxsim_backward(grad_scores, argmax, Q, q_lens, D, cu_seqlens, *, dQ=None, d
                                  _ptr(dQ), _ptr(dD), _ptr(workspace), workspace.numel(),
                                  _stream(stream))
     _check("maxsim_backward", st)
+    return dQ, dD
+
+
+def maxsim_forward_with_counts(Q, q_lens, D, cu_seqlens, *, scores=None, argmax=None, workspace=None,
+                               backward_workspace=None, stream=None):
+    """C: ``maxsim_forward_with_counts`` -- the training forward (FP16/BF16):
+    scores and argmax as ``maxsim_forward``, plus the backward's CSR source
+    counts in ``backward_workspace``.  Returns (scores, argmax,
+    backward_workspace); pass the last two to ``maxsim_backward_with_counts``."""
+    torch = _torch()
+    lib = load_library()
+    _require(Q, "Q")
+    dev = Q.device
+    _require(D, "D", dtype=Q.dtype, device=dev)
+    _require(q_lens, "q_lens", torch.int32, dev)
+    _require(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    n_q, lq_max, dim = Q.shape
+    n_docs = cu_seqlens.numel() - 1
+    total = D.shape[0]
+    code = _dtype_code(Q)
+    if scores is None:
+        scores = torch.empty((n_q, n_docs), dtype=torch.float32, device=dev)
+    if argmax is None:
+        argmax = torch.empty((n_q, n_docs, lq_max), dtype=torch.int32, device=dev)
+    ws_bytes = maxsim_forward_workspace_size(n_q, lq_max, n_docs, code, dim)
+    if ws_bytes and (workspace is None or workspace.numel() < ws_bytes):
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    bws_bytes = maxsim_backward_workspace_size(n_q, lq_max, n_docs, total)
+    if backward_workspace is None or backward_workspace.numel() < bws_bytes:
+        backward_workspace = torch.empty(max(bws_bytes, 1), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.maxsim_forward_with_counts(_ptr(Q), _ptr(q_lens), n_q, lq_max, _ptr(D), _ptr(cu_seqlens), n_docs,
+                                            total, dim, code, _ptr(scores), _ptr(argmax), _ptr(workspace),
+                                            workspace.numel() if workspace is not None else 0,
+                                            _ptr(backward_workspace), backward_workspace.numel(), _stream(stream))
+    _check("maxsim_forward_with_counts", st)
+    return scores, argmax, backward_workspace
+
+
+def maxsim_backward_with_counts(grad_scores, argmax, Q, q_lens, D, cu_seqlens, backward_workspace, *, dQ=None,
+                                dD=None, stream=None):
+    """C: ``maxsim_backward_with_counts`` -- ``maxsim_backward`` using the
+    counts ``maxsim_forward_with_counts`` left in ``backward_workspace``
+    (which this call consumes).  Returns (dQ, dD) float32."""
+    torch = _torch()
+    lib = load_library()
+    _require(grad_scores, "grad_scores", torch.float32)
+    dev = grad_scores.device
+    n_q, lq_max, dim = Q.shape
+    n_docs = cu_seqlens.numel() - 1
+    total = D.shape[0]
+    if dQ is None:
+        dQ = torch.empty((n_q, lq_max, dim), dtype=torch.float32, device=dev)
+    if dD is None:
+        dD = torch.empty((total, dim), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.maxsim_backward_with_counts(_ptr(grad_scores), _ptr(argmax), _ptr(Q), _ptr(q_lens), n_q, lq_max,
+                                             _ptr(D), _ptr(cu_seqlens), n_docs, total, dim, _dtype_code(Q),
+                                             _ptr(dQ), _ptr(dD), _ptr(backward_workspace),
+                                             backward_workspace.numel(), _stream(stream))
+    _check("maxsim_backward_with_counts", st)
     return dQ, dD
 
 

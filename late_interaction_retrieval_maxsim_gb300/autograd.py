@@ -1,12 +1,13 @@
 """``torch.autograd`` entry point over the C ABI.
 
 "FLASH-MAXSIM: IO-Aware Fused Kernels for Late-Interaction Retrieval"
-(arXiv 2605.29517) §4.2.2 builds the inverse-grid CSR "at runtime, inside
-autograd": the forward saves its argmax, and the backward turns it into dQ and
-dD without materialising the similarity tensor.  ``maxsim`` wraps exactly
-that: the forward is ``maxsim_forward`` (argmax kept for the backward), the
-backward ``maxsim_backward``.  Both run in the library's CUDA kernels; this
-module only routes tensors.
+(arXiv 2605.29517) §4.2.2 derives the inverse-grid CSR during the training
+step itself: the forward saves its argmax, and the backward turns it into dQ
+and dD without materialising the similarity tensor.  ``maxsim`` wraps exactly
+that: the forward is ``maxsim_forward_with_counts`` (argmax kept for the
+backward, and the CSR's source counts taken while it is produced), the
+backward ``maxsim_backward_with_counts``.  Both run in the library's CUDA
+kernels; this module only routes tensors.
 
 Gradients are computed in FP32 by the kernels and returned in the inputs'
 dtype (autograd requires it); pass ``fp32_grads=True`` to keep the FP32
@@ -16,7 +17,7 @@ from __future__ import annotations
 
 import torch
 
-from . import maxsim_backward, maxsim_forward
+from . import maxsim_backward, maxsim_backward_with_counts, maxsim_forward_with_counts
 
 
 class MaxSimFunction(torch.autograd.Function):
@@ -25,14 +26,20 @@ class MaxSimFunction(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, Q, D, q_lens, cu_seqlens):
-        scores, argmax, _ = maxsim_forward(Q, q_lens, D, cu_seqlens, with_argmax=True)
+        scores, argmax, bws = maxsim_forward_with_counts(Q, q_lens, D, cu_seqlens)
         ctx.save_for_backward(Q, D, q_lens, cu_seqlens, argmax)
+        ctx.backward_workspace = bws   # holds the CSR source counts; used up by one backward
         return scores
 
     @staticmethod
     def backward(ctx, grad_scores):
         Q, D, q_lens, cu_seqlens, argmax = ctx.saved_tensors
-        dQ, dD = maxsim_backward(grad_scores.float().contiguous(), argmax, Q, q_lens, D, cu_seqlens)
+        g = grad_scores.float().contiguous()
+        if ctx.backward_workspace is not None:
+            dQ, dD = maxsim_backward_with_counts(g, argmax, Q, q_lens, D, cu_seqlens, ctx.backward_workspace)
+            ctx.backward_workspace = None
+        else:   # a second backward through the same graph: count again from the argmax
+            dQ, dD = maxsim_backward(g, argmax, Q, q_lens, D, cu_seqlens)
         return (dQ.to(Q.dtype) if ctx.needs_input_grad[0] else None,
                 dD.to(D.dtype) if ctx.needs_input_grad[1] else None, None, None)
 

@@ -28,6 +28,7 @@ namespace {
 constexpr int kCsrWarps = 8;
 constexpr int kCsrThreads = 32 * kCsrWarps;
 constexpr int kCsrSmemBytes = 96 * 1024;   // per-warp histograms of one document chunk
+static_assert(kCsrSmemBytes / 4 == kCsrMaxDocTokens, "the forward's counts and the CSR agree on long documents");
 // Documents of at most kCsrSmallDoc tokens (every workload here) run in a
 // first launch with small shared-memory footprints, so many CTAs share an SM;
 // longer ones run in a second launch with the full 96 KB.
@@ -378,20 +379,25 @@ int csr_chunks(int32_t n_q, int32_t lq_max, int32_t n_docs) {
     return static_cast<int>(c < 1 ? 1 : c);
 }
 
-cudaError_t launch_build_csr(const BwdParams &p, cudaStream_t stream) {
+cudaError_t launch_build_csr(const BwdParams &p, cudaStream_t stream, bool counts_ready) {
     if (p.n_docs == 0) {
         return cudaMemsetAsync(p.row_ptr, 0, sizeof(int32_t) * (p.total_tokens + 1), stream);
     }
-    cudaError_t e = cudaMemsetAsync(p.doc_count, 0, sizeof(int32_t) * (p.n_docs + 1), stream);
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
     const unsigned grid = static_cast<unsigned>(p.n_docs) * p.chunks;
     // a document longer than kCsrSmallDoc needs a second, large-footprint launch
     const bool any_large = p.total_tokens > kCsrSmallDoc;
-    if ((e = cudaFuncSetAttribute(csr_chunk_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  kCsrSmemBytes)) != cudaSuccess)
-        return e;
-    csr_chunk_hist_kernel<<<grid, 256, kCsrSmallHistBytes, stream>>>(p, false);
-    if (any_large) csr_chunk_hist_kernel<<<grid, 256, kCsrSmemBytes, stream>>>(p, true);
+    if (!counts_ready) {
+        if ((e = cudaMemsetAsync(p.doc_count, 0, sizeof(int32_t) * (p.n_docs + 1), stream)) != cudaSuccess)
+            return e;
+        if ((e = cudaFuncSetAttribute(csr_chunk_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      kCsrSmemBytes)) != cudaSuccess)
+            return e;
+        csr_chunk_hist_kernel<<<grid, 256, kCsrSmallHistBytes, stream>>>(p, false);
+        if (any_large) csr_chunk_hist_kernel<<<grid, 256, kCsrSmemBytes, stream>>>(p, true);
+    }
+    // (with counts from the forward, documents too long for the CSR are
+    // reported by csr_place_kernel)
     csr_doc_scan_kernel<<<1, 1024, 0, stream>>>(p);
     csr_token_scan_kernel<<<p.n_docs, 256, 0, stream>>>(p);
     if ((e = cudaFuncSetAttribute(csr_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -23,6 +23,9 @@ struct FwdParams {
     int32_t *argmax;     // [n_q, ld_out, lq_max] or null
     const float *q_tok_scale;  // INT8 per-token mode: [n_q, lq_max] query-token scales
     const float *d_tok_scale;  // INT8 per-token mode: [total_tokens] document-token scales
+    int32_t *csr_cnt;          // training mode (or null): per-(document, chunk, token) source counts
+    int32_t *csr_doc_count;    // training mode: sources per document
+    int32_t csr_chunks, csr_chunk_len;
     int32_t *status;     // device status word
     int32_t n_q, lq_max, lq_pad, n_docs;
     int32_t total_tokens;
@@ -109,7 +112,12 @@ inline void make_divisor(int32_t d, uint32_t &m, uint32_t &s) {
     m = static_cast<uint32_t>(((uint64_t{1} << (31 + s)) + static_cast<uint64_t>(d) - 1) / static_cast<uint64_t>(d));
 }
 int csr_chunks(int32_t n_q, int32_t lq_max, int32_t n_docs);
-cudaError_t launch_build_csr(const BwdParams &p, cudaStream_t stream);
+// Longest document the CSR build handles (its shared-memory histograms);
+// longer ones get empty rows and a status code.
+constexpr int kCsrMaxDocTokens = 24 * 1024;
+// counts_ready: doc_count and chunk_cnt were filled by the forward (training
+// mode), so the histogram pass is skipped.
+cudaError_t launch_build_csr(const BwdParams &p, cudaStream_t stream, bool counts_ready = false);
 cudaError_t launch_grad_d(const BwdParams &p, cudaStream_t stream);
 cudaError_t launch_grad_q(const BwdParams &p, cudaStream_t stream);
 

@@ -816,12 +816,11 @@ maxsim_status_t maxsim_build_csr(const int32_t *argmax, const int32_t *q_lens, i
     return cuda_status(launch_build_csr(p, stream));
 }
 
-maxsim_status_t maxsim_backward(const float *grad_scores, const int32_t *argmax, const void *Q,
-                                const int32_t *q_lens, int32_t n_q, int32_t lq_max, const void *D,
-                                const int32_t *cu_seqlens, int32_t n_docs, int64_t total_d_tokens,
-                                int32_t dim, maxsim_dtype_t dtype, float *dQ, float *dD, void *workspace,
-                                size_t workspace_bytes, void *stream_) {
-    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+static maxsim_status_t backward_impl(const float *grad_scores, const int32_t *argmax, const void *Q,
+                                     const int32_t *q_lens, int32_t n_q, int32_t lq_max, const void *D,
+                                     const int32_t *cu_seqlens, int32_t n_docs, int64_t total_d_tokens,
+                                     int32_t dim, maxsim_dtype_t dtype, float *dQ, float *dD, void *workspace,
+                                     size_t workspace_bytes, cudaStream_t stream, bool counts_ready) {
     if (dtype == MAXSIM_INT8) return MAXSIM_ERR_UNSUPPORTED;
     if (dtype != MAXSIM_FP16 && dtype != MAXSIM_BF16) return MAXSIM_ERR_UNSUPPORTED;
     if (dim != kDim) return MAXSIM_ERR_UNSUPPORTED;
@@ -846,10 +845,67 @@ maxsim_status_t maxsim_backward(const float *grad_scores, const int32_t *argmax,
     p.dQ = dQ;
     p.dD = dD;
     p.bf16 = dtype == MAXSIM_BF16;
-    cudaError_t e = launch_build_csr(p, stream);
+    cudaError_t e = launch_build_csr(p, stream, counts_ready);
     if (e == cudaSuccess) e = launch_grad_d(p, stream);
     if (e == cudaSuccess) e = launch_grad_q(p, stream);
     return cuda_status(e);
+}
+
+maxsim_status_t maxsim_backward(const float *grad_scores, const int32_t *argmax, const void *Q,
+                                const int32_t *q_lens, int32_t n_q, int32_t lq_max, const void *D,
+                                const int32_t *cu_seqlens, int32_t n_docs, int64_t total_d_tokens,
+                                int32_t dim, maxsim_dtype_t dtype, float *dQ, float *dD, void *workspace,
+                                size_t workspace_bytes, void *stream_) {
+    return backward_impl(grad_scores, argmax, Q, q_lens, n_q, lq_max, D, cu_seqlens, n_docs, total_d_tokens, dim,
+                         dtype, dQ, dD, workspace, workspace_bytes, static_cast<cudaStream_t>(stream_), false);
+}
+
+maxsim_status_t maxsim_forward_with_counts(const void *Q, const int32_t *q_lens, int32_t n_q, int32_t lq_max,
+                                           const void *D, const int32_t *cu_seqlens, int32_t n_docs,
+                                           int64_t total_d_tokens, int32_t dim, maxsim_dtype_t dtype,
+                                           float *scores, int32_t *argmax, void *workspace,
+                                           size_t workspace_bytes, void *backward_workspace,
+                                           size_t backward_workspace_bytes, void *stream_) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (dtype != MAXSIM_FP16 && dtype != MAXSIM_BF16) return MAXSIM_ERR_UNSUPPORTED;
+    maxsim_status_t st = check_forward_args(Q, q_lens, n_q, lq_max, n_docs, total_d_tokens, dim, dtype, 1.0f,
+                                            1.0f);
+    if (st != MAXSIM_OK) return st;
+    if ((st = check_csr_args(argmax, q_lens, n_q, lq_max, cu_seqlens, n_docs, total_d_tokens)) != MAXSIM_OK)
+        return st;
+    if (n_q == 0 || n_docs == 0) return MAXSIM_OK;
+    if (!cu_seqlens || !scores || !argmax) return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (total_d_tokens > 0 && (!D || !aligned16(D))) return MAXSIM_ERR_INVALID_ARGUMENT;
+    const FwdLayout wl = forward_layout(n_q, lq_max, n_docs, dtype);
+    if (wl.total > 0 && (workspace == nullptr || workspace_bytes < wl.total)) return MAXSIM_ERR_WORKSPACE;
+    const BwdLayout bl = backward_layout(n_q, lq_max, n_docs, total_d_tokens);
+    if (backward_workspace == nullptr || backward_workspace_bytes < bl.total) return MAXSIM_ERR_WORKSPACE;
+
+    uint8_t *bws = static_cast<uint8_t *>(backward_workspace);
+    int32_t *doc_count = reinterpret_cast<int32_t *>(bws + bl.row_ptr + bl.col_idx);
+    int32_t *chunk_cnt = reinterpret_cast<int32_t *>(bws + bl.row_ptr + bl.col_idx + bl.doc_count);
+    // the counts start at zero (doc_count and chunk_cnt are adjacent)
+    if (cudaMemsetAsync(doc_count, 0, bl.doc_count + bl.chunk_cnt, stream) != cudaSuccess) return MAXSIM_ERR_CUDA;
+    ForwardPlan plan;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    st = forward_prepare(plan, Q, q_lens, n_q, lq_max, dtype, 1.0f, 1.0f, ws, ws + wl.partials, stream);
+    if (st != MAXSIM_OK) return st;
+    const int chunks = csr_chunks(n_q, lq_max, n_docs);
+    const int64_t n_cand = static_cast<int64_t>(n_q) * lq_max;
+    plan.p.csr_cnt = chunk_cnt;
+    plan.p.csr_doc_count = doc_count;
+    plan.p.csr_chunks = chunks;
+    plan.p.csr_chunk_len = static_cast<int32_t>(std::max<int64_t>(1, (n_cand + chunks - 1) / chunks));
+    return forward_block(plan, D, cu_seqlens, n_docs, total_d_tokens, scores, nullptr, argmax, n_docs, stream);
+}
+
+maxsim_status_t maxsim_backward_with_counts(const float *grad_scores, const int32_t *argmax, const void *Q,
+                                            const int32_t *q_lens, int32_t n_q, int32_t lq_max, const void *D,
+                                            const int32_t *cu_seqlens, int32_t n_docs, int64_t total_d_tokens,
+                                            int32_t dim, maxsim_dtype_t dtype, float *dQ, float *dD,
+                                            void *workspace, size_t workspace_bytes, void *stream_) {
+    return backward_impl(grad_scores, argmax, Q, q_lens, n_q, lq_max, D, cu_seqlens, n_docs, total_d_tokens, dim,
+                         dtype, dQ, dD, workspace, workspace_bytes, static_cast<cudaStream_t>(stream_), true);
 }
 
 maxsim_status_t maxsim_device_status(void *stream_, int32_t clear, int32_t *code) {

@@ -116,3 +116,35 @@ def test_out_of_range_argmax_is_reported(ops):
     ops.maxsim_build_csr(argmax, ql, cu, D.shape[0])
     assert ops.maxsim_device_status(clear=True) == 0x201
     assert ops.maxsim_device_status() == 0
+
+
+def _counted_matches_plain(ops, Q, ql, D, cu):
+    s0, a0, _ = ops.maxsim_forward(Q, ql, D, cu)
+    s1, a1, bws = ops.maxsim_forward_with_counts(Q, ql, D, cu)
+    torch.cuda.synchronize()
+    assert ops.maxsim_device_status() == 0
+    assert torch.equal(s0, s1) and torch.equal(a0, a1)
+    g = torch.where(torch.isfinite(s0), s0, torch.zeros_like(s0))
+    g = torch.softmax(g / 0.05, dim=1).contiguous()
+    dq0, dd0 = ops.maxsim_backward(g, a0, Q, ql, D, cu)
+    dq1, dd1 = ops.maxsim_backward_with_counts(g, a1, Q, ql, D, cu, bws)
+    torch.cuda.synchronize()
+    assert ops.maxsim_device_status() == 0
+    assert torch.equal(dq0, dq1) and torch.equal(dd0, dd1)
+
+
+@pytest.mark.parametrize("case", ["train", "ragged", "long", "chunked"])
+def test_counting_forward_and_counted_backward(ops, case):
+    """The training pair: the forward counts the CSR's sources while it
+    writes the argmax; the backward that uses those counts gives the same
+    bits as the one that counts from the argmax itself."""
+    if case == "train":
+        x = syn.make_inputs(syn.WORKLOADS["train"], device="cuda")
+        Q, ql, D, cu = x["Q"], x["q_lens"], x["D"], x["cu_seqlens"]
+    elif case == "ragged":
+        Q, ql, D, cu = random_case(4, 40, [5, 0, 130, 1, 257, 0, 33], "fp16", [40, 0, 17, 33], seed=51)
+    elif case == "long":
+        Q, ql, D, cu = random_case(3, 300, [700, 64, 3, 1024], "bf16", [300, 129, 1], seed=52)
+    else:
+        Q, ql, D, cu = random_case(16, 1024, [1024] * 6 + [3, 700], "bf16", [1024] * 12 + [1, 0, 512, 700], seed=53)
+    _counted_matches_plain(ops, Q, ql, D, cu)

@@ -62,3 +62,21 @@ def test_autograd_grads_equal_the_c_abi_backward(ops):
     dQ, dD = ops.maxsim_backward(g.contiguous(), am, Q, ql, D, cu)
     assert torch.equal(Qa.grad, dQ.to(torch.bfloat16))
     assert torch.equal(Da.grad, dD.to(torch.bfloat16))
+
+
+def test_autograd_second_backward_through_the_same_graph(ops):
+    """The first backward uses (and consumes) the forward's CSR counts; a
+    second one through the retained graph counts from the argmax and must
+    give the same gradients."""
+    from late_interaction_retrieval_maxsim_gb300.autograd import maxsim
+    Q, ql, D, cu = random_case(4, 32, [180] * 8, "bf16", seed=79)
+    Qa = Q.clone().requires_grad_(True)
+    Da = D.clone().requires_grad_(True)
+    s = maxsim(Qa, Da, ql, cu)
+    g = torch.softmax(s.detach() / 0.05, dim=1)
+    s.backward(g, retain_graph=True)
+    gq, gd = Qa.grad.clone(), Da.grad.clone()
+    Qa.grad = None
+    Da.grad = None
+    s.backward(g)
+    assert torch.equal(Qa.grad, gq) and torch.equal(Da.grad, gd)
