@@ -429,11 +429,11 @@ int chamfer_slices(int32_t n_items, int32_t max_s, int32_t max_t, int sm_count) 
     // CTAs = items x source tiles x slices run in waves of `slots` (two per
     // SM); a CTA's time is proportional to its slice, 1 / s of the targets,
     // so the search takes ceil(ctas / slots) / s.  Take the smallest s within
-    // 5 % of the best (fewer, larger CTAs; each slice keeps at least 2,048
-    // targets, at most 64 slices).
+    // 5 % of the best (fewer, larger CTAs; each slice keeps at least one
+    // shared-memory tile of targets, at most 64 slices).
     const int64_t tiles = static_cast<int64_t>(n_items) * ((max_s + kNnSources - 1) / kNnSources);
     const int64_t slots = 2LL * std::max(sm_count, 1);
-    const int64_t cap = std::max<int64_t>(1, std::min<int64_t>(64, max_t / 2048));
+    const int64_t cap = std::max<int64_t>(1, std::min<int64_t>(64, max_t / kNnTile));
     if (tiles <= 0) return 1;
     auto cost = [&](int64_t sl) {
         return static_cast<double>((tiles * sl + slots - 1) / slots) / static_cast<double>(sl);
