@@ -191,3 +191,65 @@ def test_two_stage_rerank_fewer_documents_than_candidates(ops):
     assert np.all(ids[:, 5:] == -1) and np.all(np.isneginf(scores[:, 5:].cpu().numpy()))
     assert all(sorted(ids[q, :5].tolist()) == [0, 1, 2, 3, 4] for q in range(2))
     assert np.all(cand[:, 5:].cpu().numpy() == -1)
+
+
+def test_int8_per_token_full_size_sampled(ops):
+    """The INT8 varlen workload at full size (32 x 32 queries vs 100,000
+    documents, Ld ~ U[32, 512]) with per-token scales: argmax bit-exact and
+    scores within tolerance on 40 sampled documents."""
+    w = syn.WORKLOADS["int8_varlen"]
+    cu = syn.cu_seqlens_from_lengths(syn.doc_lengths(w.n_docs, w.ld_lo, w.ld_hi, w.seed))
+    total = int(cu[-1])
+    Q8, qs = syn.unit_tokens_int8_per_token(w.n_q * w.lq, 128, w.seed + 1, "cuda")
+    D8, ds = syn.unit_tokens_int8_per_token(total, 128, w.seed + 2, "cuda")
+    Q8, qs = Q8.view(w.n_q, w.lq, 128), qs.view(w.n_q, w.lq)
+    ql = torch.full((w.n_q,), w.lq, dtype=torch.int32, device="cuda")
+    s, a = ops.maxsim_forward_int8_per_token(Q8, qs, ql, D8, ds, cu.cuda())
+    torch.cuda.synchronize()
+    assert ops.maxsim_device_status() == 0
+    rng = np.random.default_rng(3)
+    docs = sorted(set(rng.integers(0, w.n_docs, 36).tolist()) | {0, 1, w.n_docs - 2, w.n_docs - 1})
+    cu_h = cu.numpy()
+    pieces = [D8[int(cu_h[b]):int(cu_h[b + 1])] for b in docs]
+    sc = [ds[int(cu_h[b]):int(cu_h[b + 1])] for b in docs]
+    cu_sub = np.concatenate([[0], np.cumsum([p.shape[0] for p in pieces])]).astype(np.int32)
+    ref = oracle.forward_i8_token(Q8.cpu().numpy(), qs.cpu().numpy(), ql.cpu().numpy(),
+                                  torch.cat(pieces).cpu().numpy(), torch.cat(sc).cpu().numpy(), cu_sub,
+                                  threads=THREADS)
+    idx = torch.as_tensor(docs)
+    assert np.array_equal(a[:, idx].cpu().numpy(), ref["argmax"].reshape(w.n_q, len(docs), w.lq))
+    err = np.abs(s[:, idx].double().cpu().numpy() - ref["score"].reshape(w.n_q, len(docs)))
+    assert err.max() <= SCORE_TOL_PER_TOKEN * w.lq
+
+
+def test_two_stage_rerank_full_size_sampled(ops):
+    """The scan at the benchmark's size (32 x 32 queries vs 100,000 documents,
+    1,000 candidates, 100 kept): the candidates are exactly the row-wise
+    top-1000 of the INT8 scores (a property at any size), and sampled final
+    scores match the oracle's FP16 rescoring."""
+    w = syn.WORKLOADS["int8_varlen"]
+    cu = syn.cu_seqlens_from_lengths(syn.doc_lengths(w.n_docs, w.ld_lo, w.ld_hi, w.seed))
+    total = int(cu[-1])
+    Q8, qs = syn.unit_tokens_int8(w.n_q * w.lq, 128, w.seed + 1, "cuda")
+    D8, ds = syn.unit_tokens_int8(total, 128, w.seed + 2, "cuda")
+    Q8 = Q8.view(w.n_q, w.lq, 128)
+    Q16 = syn.unit_tokens(w.n_q * w.lq, 128, w.seed + 1, "fp16", "cuda").view(w.n_q, w.lq, 128)
+    D16 = syn.unit_tokens(total, 128, w.seed + 2, "fp16", "cuda")
+    ql = torch.full((w.n_q,), w.lq, dtype=torch.int32, device="cuda")
+    cu_d = cu.cuda()
+    ids, scores, cand = ops.maxsim_rerank_two_stage(Q8, D8, Q16, D16, ql, cu_d, k_candidates=1000, k=100,
+                                                    q_scale=qs, d_scale=ds, max_doc_len=w.ld_hi,
+                                                    return_candidates=True)
+    s1, _, _ = ops.maxsim_forward(Q8, ql, D8, cu_d, with_argmax=False, q_scale=qs, d_scale=ds)
+    top_ids, _ = ops.maxsim_topk(s1, 1000)
+    torch.cuda.synchronize()
+    assert ops.maxsim_device_status() == 0
+    assert torch.equal(cand, top_ids)
+    assert all(set(ids[q].tolist()) <= set(cand[q].tolist()) for q in range(w.n_q))
+    assert torch.all(scores[:, :-1] >= scores[:, 1:])
+    qb, db = syn.bits_u16(Q16), syn.bits_u16(D16)
+    rng = np.random.default_rng(4)
+    pairs = [(int(q), int(ids[q, j])) for q in rng.integers(0, w.n_q, 6) for j in rng.integers(0, 100, 4)]
+    ref = oracle.forward_bits("fp16", qb, ql.cpu().numpy(), db, cu.numpy(), pairs=pairs, threads=THREADS)["score"]
+    got = np.array([float(scores[q, (ids[q] == d).nonzero()[0, 0]]) for q, d in pairs])
+    assert np.abs(got - ref).max() <= SCORE_TOL_PER_TOKEN * w.lq
