@@ -235,7 +235,7 @@ __device__ __forceinline__ void epilogue_warp(const FwdParams &p, int rho_warp, 
                                               uint32_t tmem_base, int qd, int b_begin, int b_end,
                                               int t_begin, int t_end, int n_tiles, uint64_t *t_full,
                                               float *scale_slot, SlotOf slot_of, Release release,
-                                              volatile int32_t *abort_flag, bool cluster_scope) {
+                                              volatile int32_t *abort_flag) {
     const int lane = threadIdx.x & 31;
     const bool warp_rows = rho_warp < rows_total;
     const int rho = rho_warp + lane;
@@ -390,8 +390,7 @@ __device__ __forceinline__ void epilogue_warp(const FwdParams &p, int rho_warp, 
         const int2 su = slot_of(j);
         const int slot = su.x;
         const uint32_t use = static_cast<uint32_t>(su.y);
-        if (!(cluster_scope ? mbar_wait_cluster(&t_full[slot], use & 1, abort_flag, p.status, kStatusTimeoutEpilogue)
-                            : mbar_wait(&t_full[slot], use & 1, abort_flag, p.status, kStatusTimeoutEpilogue))) {
+        if (!mbar_wait(&t_full[slot], use & 1, abort_flag, p.status, kStatusTimeoutEpilogue)) {
             aborted = true;
             break;
         }

@@ -277,7 +277,7 @@ maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                 p, row0 + mt * 128 + qd * 32, rows_total, tmem_base, qd, b_begin, b_end, t_begin, t_end,
                 n_tiles, ctl->t_full, ctl->scale_buf[warp - C::kFirstEpiWarp],
                 [&](int j) { return make_int2(mt + NMT * (j % (kSlots / NMT)), j / (kSlots / NMT)); },
-                [&](int slot) { mbar_arrive(&ctl->t_empty[slot]); }, abort_flag, false);
+                [&](int slot) { mbar_arrive(&ctl->t_empty[slot]); }, abort_flag);
         }
     }
 
