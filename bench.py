@@ -189,7 +189,7 @@ def _extra_workloads(m, syn, rl, peaks):
     import torch
     out = {}
     stream = torch.cuda.current_stream()
-    for name in ("colpali", "train", "train_colpali", "int8_varlen"):
+    for name in ("colbert_1q", "colpali", "train", "train_colpali", "int8_varlen"):
         w = syn.WORKLOADS[name]
         x = syn.make_inputs(w, device="cuda")
         Q, ql, D, cu = x["Q"], x["q_lens"], x["D"], x["cu_seqlens"]
@@ -205,6 +205,13 @@ def _extra_workloads(m, syn, rl, peaks):
                "dtype": w.dtype, "fwd_ms": round(ms, 4), "docs_per_s": w.n_docs / (ms / 1e3),
                "fwd_tflops": flops / (ms / 1e3) / 1e12,
                "fwd_frac_of_measured_bf16_peak": flops / (ms / 1e3) / 1e12 / peaks["bf16_tflops"]}
+        if name == "colbert_1q":
+            # one query: 32 FLOP per document byte, far below the ridge -- HBM-bound
+            hb = rl.forward_hbm_bytes(w.n_q, w.lq, w.n_docs, D.shape[0])
+            rec["roofline"] = {"bound": "hbm", "achieved": round(hb / (ms / 1e3) / 1e9, 1),
+                               "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                               "frac": round(hb / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 3),
+                               "algorithmic_bytes_per_launch": hb}
         if name.startswith("train"):
             n = s.shape[0]
             g = torch.softmax(s / 0.05, dim=1)

@@ -44,8 +44,7 @@ using namespace ptx;
 constexpr int kKBlockBytes = 128 * 128;        // 128 rows x 64 16-bit elements, 128B-swizzled
 constexpr int kTileBytes = 2 * kKBlockBytes;   // 128 rows x 128 16-bit elements
 constexpr int kI8TileBytes = 128 * 128;        // 128 rows x 128 int8
-constexpr int kSlots = 4;                      // TMEM accumulator slots
-constexpr int kTmemCols = kSlots * kSlotCols;  // 512: the whole TMEM
+constexpr int kMaxSlots = 4;                   // TMEM accumulator slots (4 x 128 columns: all of TMEM)
 
 constexpr int kMaxStages = 4;
 
@@ -57,8 +56,8 @@ struct SharedCtl {
     uint64_t d_empty[kMaxStages];   // FP16 D stage consumed by the MMA
     uint64_t i_full[kMaxStages];    // INT8 staging tile landed
     uint64_t i_empty[kMaxStages];   // INT8 staging tile converted
-    uint64_t t_full[kSlots];
-    uint64_t t_empty[kSlots];
+    uint64_t t_full[kMaxSlots];
+    uint64_t t_empty[kMaxSlots];
     uint64_t mma_done;
     uint32_t tmem_base;
     int32_t abort;
@@ -68,7 +67,13 @@ struct SharedCtl {
 
 template <int NMT, bool INT8>
 struct Cfg {
-    static constexpr int kStages = INT8 ? (NMT == 4 ? 2 : 3) : (NMT == 4 ? 3 : 4);
+    // One 16-bit M-tile (a few short queries, a single-query rerank): two CTAs
+    // share an SM, each with half of TMEM (2 slots) and 2 document stages, so
+    // two epilogue warps with valid rows run per SM instead of one.
+    static constexpr int kCtasPerSm = (NMT == 1 && !INT8) ? 2 : 1;
+    static constexpr int kSlots = kCtasPerSm == 2 ? 2 : 4;
+    static constexpr int kTmemCols = kSlots * kSlotCols;
+    static constexpr int kStages = INT8 ? (NMT == 4 ? 2 : 3) : (NMT == 4 ? 3 : (kCtasPerSm == 2 ? 2 : 4));
     static constexpr int kI8Stages = INT8 ? (NMT == 4 ? 2 : 4) : 0;
     static constexpr int kConvWarps = INT8 ? (NMT == 4 ? 2 : 4) : 0;
     static constexpr bool kDoubleBuffer = NMT < 4;
@@ -81,6 +86,9 @@ struct Cfg {
     static_assert(kStages >= 1 && kStages <= kMaxStages, "barrier arrays hold kMaxStages stages");
     static_assert(kI8Stages <= kMaxStages, "barrier arrays hold kMaxStages stages");
     static_assert(kSmem <= 232448, "exceeds the 227 KB shared-memory limit per CTA");
+    static_assert(kSlots <= kMaxSlots && kSlots % NMT == 0, "slots hold whole row groups");
+    // at most kCtasPerSm CTAs fit an SM's 228 KB, so their TMEM never exceeds 512 columns
+    static_assert(kCtasPerSm == 1 || 3 * (kSmem + 1024) > 233472, "a third CTA could oversubscribe TMEM");
 };
 
 // int8 x4 -> fp16 x4 exactly: (x ^ 0x80) in the low byte of 1024.0 gives
@@ -96,7 +104,7 @@ __device__ __forceinline__ uint2 widen_i8x4(uint32_t w) {
 }
 
 template <int NMT, bool ARGMAX, bool INT8, bool SCALE, bool COUNT>
-__global__ void __launch_bounds__(Cfg<NMT, INT8>::kThreads, 1)
+__global__ void __launch_bounds__(Cfg<NMT, INT8>::kThreads, Cfg<NMT, INT8>::kCtasPerSm)
 maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmD,
                   const FwdParams p) {
     using C = Cfg<NMT, INT8>;
@@ -126,7 +134,7 @@ maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             mbar_init(&ctl->i_full[s], 1);
             mbar_init(&ctl->i_empty[s], INT8 ? 32 * C::kConvWarps : 1);
         }
-        for (int s = 0; s < kSlots; ++s) {
+        for (int s = 0; s < C::kSlots; ++s) {
             mbar_init(&ctl->t_full[s], 1);
             mbar_init(&ctl->t_empty[s], 4);
         }
@@ -146,7 +154,7 @@ maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         ctl->t_end = p.cu_seqlens[max(bb, be)];
     }
     if (warp == 1) {
-        tmem_alloc(&ctl->tmem_base, kTmemCols);
+        tmem_alloc(&ctl->tmem_base, C::kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -214,8 +222,8 @@ maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                 tc_fence_after();
                 const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((s * kTileBytes) >> 4);
                 for (int mt = 0; mt < n_mt; ++mt) {
-                    const int slot = mt + NMT * (j % (kSlots / NMT));
-                    const uint32_t use = j / (kSlots / NMT);
+                    const int slot = mt + NMT * (j % (C::kSlots / NMT));
+                    const uint32_t use = j / (C::kSlots / NMT);
                     if (!mbar_wait(&ctl->t_empty[slot], (use & 1) ^ 1, abort_flag, p.status, kStatusTimeoutMma)) {
                         ok = false;
                         break;
@@ -276,7 +284,7 @@ maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             epilogue_warp<ARGMAX, INT8 && !SCALE, SCALE, C::kDoubleBuffer, COUNT>(
                 p, row0 + mt * 128 + qd * 32, rows_total, tmem_base, qd, b_begin, b_end, t_begin, t_end,
                 n_tiles, ctl->t_full, ctl->scale_buf[warp - C::kFirstEpiWarp],
-                [&](int j) { return make_int2(mt + NMT * (j % (kSlots / NMT)), j / (kSlots / NMT)); },
+                [&](int j) { return make_int2(mt + NMT * (j % (C::kSlots / NMT)), j / (C::kSlots / NMT)); },
                 [&](int slot) { mbar_arrive(&ctl->t_empty[slot]); }, abort_flag);
         }
     }
@@ -285,7 +293,7 @@ maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+    if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
 }
 
 // Sum the per-32-token-chunk partials of queries longer than 32 tokens, in
@@ -364,6 +372,11 @@ int grid_for(int64_t n, int threads) {
 int forward_smem_bytes(int nmt, bool int8) {
     if (int8) return nmt == 1 ? Cfg<1, true>::kSmem : nmt == 2 ? Cfg<2, true>::kSmem : Cfg<4, true>::kSmem;
     return nmt == 1 ? Cfg<1, false>::kSmem : nmt == 2 ? Cfg<2, false>::kSmem : Cfg<4, false>::kSmem;
+}
+
+int forward_ctas_per_sm(int nmt, bool int8) {
+    if (int8) return 1;
+    return nmt == 1 ? Cfg<1, false>::kCtasPerSm : nmt == 2 ? Cfg<2, false>::kCtasPerSm : Cfg<4, false>::kCtasPerSm;
 }
 
 int forward_threads(int nmt, bool int8) {

@@ -41,6 +41,7 @@ inline int forward_mtiles(int64_t rows) { return rows <= 128 ? 1 : rows <= 256 ?
 // fwd_tc.cu
 int forward_smem_bytes(int nmt, bool int8);
 int forward_threads(int nmt, bool int8);
+int forward_ctas_per_sm(int nmt, bool int8);   // CTAs one SM runs at once
 // Forward arithmetic: FP16/BF16 MMA on the inputs; INT8 with one scale per
 // tensor (exact integer maxima, int64 sums); INT8 with one scale per token
 // (exact integer dots scaled per document token in FP32 before the maximum,

@@ -313,7 +313,8 @@ maxsim_status_t forward_block(ForwardPlan &plan, const void *D, const int32_t *c
     // into token-balanced parts, one CTA per (group, part).
     const int64_t rows = static_cast<int64_t>(p.n_q) * p.lq_pad;
     const int64_t groups = (rows + plan.nmt * 128 - 1) / (plan.nmt * 128);
-    const int64_t parts = std::max<int64_t>(1, plan.sm_count / groups);
+    const int64_t parts =
+        std::max<int64_t>(1, static_cast<int64_t>(forward_ctas_per_sm(plan.nmt, plan.int8)) * plan.sm_count / groups);
     if (groups * parts > INT32_MAX) return MAXSIM_ERR_INVALID_ARGUMENT;
     p.groups = static_cast<int32_t>(groups);
     p.parts = static_cast<int32_t>(parts);

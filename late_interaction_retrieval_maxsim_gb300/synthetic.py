@@ -53,6 +53,8 @@ WORKLOADS = {
                      note="1 query Lq=32 vs 256 docs Ld=128, FP16"),
     "colbert_varlen": Workload("colbert_varlen", 16, 32, 50_000, 32, 300, "fp16",
                                note="16 queries Lq=32 vs 50,000 docs Ld~U[32,300], packed"),
+    "colbert_1q": Workload("colbert_1q", 1, 32, 50_000, 32, 300, "fp16",
+                           note="1 query Lq=32 vs the 50,000 ColBERT documents (single-query rerank, HBM-bound)"),
     "colpali": Workload("colpali", 1, 1024, 10_000, 1024, 1024, "fp16",
                         note="1 query Lq=1024 vs 10,000 docs Ld=1024"),
     "train": Workload("train", 256, 32, 256, 180, 180, "bf16",
