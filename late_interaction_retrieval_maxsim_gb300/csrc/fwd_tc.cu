@@ -70,12 +70,14 @@ struct Cfg {
     // One 16-bit M-tile (a few short queries, a single-query rerank): two CTAs
     // share an SM, each with half of TMEM (2 slots) and 2 document stages, so
     // two epilogue warps with valid rows run per SM instead of one.
-    static constexpr int kCtasPerSm = (NMT == 1 && !INT8) ? 2 : 1;
+    // (INT8 too: one FP16 stage, two INT8 staging tiles and two converter
+    // warps keep it within half an SM's shared memory and registers.)
+    static constexpr int kCtasPerSm = NMT == 1 ? 2 : 1;
     static constexpr int kSlots = kCtasPerSm == 2 ? 2 : 4;
     static constexpr int kTmemCols = kSlots * kSlotCols;
-    static constexpr int kStages = INT8 ? (NMT == 4 ? 2 : 3) : (NMT == 4 ? 3 : (kCtasPerSm == 2 ? 2 : 4));
-    static constexpr int kI8Stages = INT8 ? (NMT == 4 ? 2 : 4) : 0;
-    static constexpr int kConvWarps = INT8 ? (NMT == 4 ? 2 : 4) : 0;
+    static constexpr int kStages = INT8 ? (NMT == 4 ? 2 : (NMT == 1 ? 1 : 3)) : (NMT == 4 ? 3 : (NMT == 1 ? 2 : 4));
+    static constexpr int kI8Stages = INT8 ? (NMT == 2 ? 4 : 2) : 0;
+    static constexpr int kConvWarps = INT8 ? (NMT == 2 ? 4 : 2) : 0;
     static constexpr bool kDoubleBuffer = NMT < 4;
     static constexpr int kFirstEpiWarp = 2 + kConvWarps;
     static constexpr int kThreads = 32 * (kFirstEpiWarp + 4 * NMT);
@@ -375,7 +377,7 @@ int forward_smem_bytes(int nmt, bool int8) {
 }
 
 int forward_ctas_per_sm(int nmt, bool int8) {
-    if (int8) return 1;
+    if (int8) return nmt == 1 ? Cfg<1, true>::kCtasPerSm : nmt == 2 ? Cfg<2, true>::kCtasPerSm : Cfg<4, true>::kCtasPerSm;
     return nmt == 1 ? Cfg<1, false>::kCtasPerSm : nmt == 2 ? Cfg<2, false>::kCtasPerSm : Cfg<4, false>::kCtasPerSm;
 }
 
