@@ -67,18 +67,19 @@ struct SharedCtl {
 
 template <int NMT, bool INT8>
 struct Cfg {
-    // One 16-bit M-tile (a few short queries, a single-query rerank): two CTAs
-    // share an SM, each with half of TMEM (2 slots) and 2 document stages, so
-    // two epilogue warps with valid rows run per SM instead of one.
-    // (INT8 too: one FP16 stage, two INT8 staging tiles and two converter
-    // warps keep it within half an SM's shared memory and registers.)
-    static constexpr int kCtasPerSm = NMT == 1 ? 2 : 1;
+    // One or two M-tiles: two CTAs share an SM, each with half of TMEM and of
+    // shared memory, so twice the epilogue warps with valid rows run per SM.
+    // One M-tile: 2 slots (double-buffered), 2 document stages (INT8: one FP16
+    // stage, two INT8 staging tiles, two converter warps).  Two M-tiles
+    // (16-bit only): one slot per M-tile, one document stage, single-buffered
+    // TMEM reads (five warps per scheduler leave 96 registers).
+    static constexpr int kCtasPerSm = (NMT == 1 || (NMT == 2 && !INT8)) ? 2 : 1;
     static constexpr int kSlots = kCtasPerSm == 2 ? 2 : 4;
     static constexpr int kTmemCols = kSlots * kSlotCols;
-    static constexpr int kStages = INT8 ? (NMT == 4 ? 2 : (NMT == 1 ? 1 : 3)) : (NMT == 4 ? 3 : (NMT == 1 ? 2 : 4));
+    static constexpr int kStages = INT8 ? (NMT == 4 ? 2 : (NMT == 1 ? 1 : 3)) : (NMT == 4 ? 3 : (NMT == 1 ? 2 : 1));
     static constexpr int kI8Stages = INT8 ? (NMT == 2 ? 4 : 2) : 0;
     static constexpr int kConvWarps = INT8 ? (NMT == 2 ? 4 : 2) : 0;
-    static constexpr bool kDoubleBuffer = NMT < 4;
+    static constexpr bool kDoubleBuffer = NMT == 1 || (NMT == 2 && INT8);
     static constexpr int kFirstEpiWarp = 2 + kConvWarps;
     static constexpr int kThreads = 32 * (kFirstEpiWarp + 4 * NMT);
     static constexpr int kQBytes = NMT * kTileBytes;

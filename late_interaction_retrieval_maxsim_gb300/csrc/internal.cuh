@@ -36,7 +36,16 @@ struct FwdParams {
 };
 
 // Number of 128-row M-tiles one CTA holds (1, 2 or 4) for R padded rows.
-inline int forward_mtiles(int64_t rows) { return rows <= 128 ? 1 : rows <= 256 ? 2 : 4; }
+// 16-bit: two CTAs of two M-tiles per SM, except for 257-384 rows, where one
+// CTA of four M-tiles (one of them empty) finishes sooner than two groups of
+// two.  With several row groups every group gets the same share of the SMs,
+// so a part-filled last group of four saves no time.  INT8 keeps four above 256 rows (its two-M-tile form runs one CTA
+// per SM).
+inline int forward_mtiles(int64_t rows, bool int8) {
+    if (rows <= 128) return 1;
+    if (rows <= 256) return 2;
+    return (int8 || rows <= 384) ? 4 : 2;
+}
 
 // fwd_tc.cu
 int forward_smem_bytes(int nmt, bool int8);

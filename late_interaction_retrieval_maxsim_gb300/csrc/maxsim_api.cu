@@ -273,7 +273,7 @@ maxsim_status_t forward_prepare(ForwardPlan &plan, const void *Q, const int32_t 
     plan.dtype = dtype;
     plan.sm_count = di.sm_count;
     plan.empty_q = lq_max == 0;
-    plan.nmt = forward_mtiles(static_cast<int64_t>(n_q) * lq_pad);
+    plan.nmt = forward_mtiles(static_cast<int64_t>(n_q) * lq_pad, int8);
     if (plan.empty_q) return MAXSIM_OK;
     const void *q_src = Q;
     if (int8) {

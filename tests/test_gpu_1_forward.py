@@ -61,6 +61,24 @@ def test_many_queries_several_groups(ops):
     check_forward("bf16", Q, ql, D, cu, scores, argmax)
 
 
+@pytest.mark.parametrize("n_q", [9, 12, 16, 20])
+def test_row_group_shapes(ops, n_q):
+    """Row counts that pick each M-tile layout: 288 and 384 padded rows run
+    one four-M-tile CTA per SM with one or more empty M-tiles; 512 and 640
+    rows run two CTAs of two M-tiles per SM, 640 with a half-empty last
+    group.  Ragged documents and queries, with and without the argmax."""
+    rng = np.random.default_rng(40 + n_q)
+    lengths = rng.integers(0, 400, 300).tolist()
+    q_lens = rng.integers(1, 33, n_q).tolist()
+    q_lens[-1] = 32
+    Q, ql, D, cu = random_case(n_q, 32, lengths, "fp16", q_lens, seed=n_q)
+    scores, argmax, _ = ops.maxsim_forward(Q, ql, D, cu)
+    assert ops.maxsim_device_status() == 0
+    check_forward("fp16", Q, ql, D, cu, scores, argmax)
+    s2, _, _ = ops.maxsim_forward(Q, ql, D, cu, with_argmax=False)
+    assert torch.equal(scores, s2)
+
+
 def test_without_argmax_same_scores(ops):
     Q, ql, D, cu = random_case(3, 32, [100, 7, 300, 129, 0, 64], "fp16", [32, 20, 1], seed=2)
     s1, a1, _ = ops.maxsim_forward(Q, ql, D, cu)
