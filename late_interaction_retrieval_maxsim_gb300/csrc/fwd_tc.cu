@@ -80,6 +80,10 @@ struct Cfg {
     static constexpr int kI8Stages = INT8 ? (NMT == 2 ? 4 : 2) : 0;
     static constexpr int kConvWarps = INT8 ? (NMT == 2 ? 4 : 2) : 0;
     static constexpr bool kDoubleBuffer = NMT == 1 || (NMT == 2 && INT8);
+    // A single 16-bit stage may be filled and consumed one K-block (64 of the
+    // 128 dimensions) at a time (chosen per launch): the next tile's first
+    // half loads while the MMAs of the second half run.
+    static constexpr bool kKSplit = !INT8 && kStages == 1;
     static constexpr int kFirstEpiWarp = 2 + kConvWarps;
     static constexpr int kThreads = 32 * (kFirstEpiWarp + 4 * NMT);
     static constexpr int kQBytes = NMT * kTileBytes;
@@ -169,6 +173,7 @@ maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     const int t_begin = ctl->t_begin, t_end = ctl->t_end;
     const int n_tiles = (t_end - t_begin + kBlockN - 1) / kBlockN;
     const bool run_pipeline = n_tiles > 0 && n_mt > 0;
+    const bool ksplit = C::kKSplit && p.ksplit != 0;
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
@@ -184,13 +189,20 @@ maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                 tma_load_3d(dst, &tmQ, &ctl->q_full, 0, i0, qq);
                 tma_load_3d(dst + kKBlockBytes, &tmQ, &ctl->q_full, 64, i0, qq);
             }
-            constexpr int kS = INT8 ? C::kI8Stages : C::kStages;
+            // K-split: a ring of two half-stages (one K-block each), load u =
+            // 2 * tile + K-block
+            const int kS = INT8 ? C::kI8Stages : (ksplit ? 2 : C::kStages);
+            const int n_loads = ksplit ? 2 * n_tiles : n_tiles;
             int issued = 0;
-            for (int j = 0; j < n_tiles; ++j) {
+            for (int j = 0; j < n_loads; ++j) {
                 const int s = j % kS;
                 const uint32_t ph = (j / kS) & 1;
-                const int row = t_begin + j * kBlockN;
-                if (INT8) {
+                const int row = t_begin + (ksplit ? j >> 1 : j) * kBlockN;
+                if (ksplit) {
+                    if (!mbar_wait(&ctl->d_empty[s], ph ^ 1, abort_flag, p.status, kStatusTimeoutProducer)) break;
+                    mbar_arrive_expect_tx(&ctl->d_full[s], kKBlockBytes);
+                    tma_load_2d(sD + s * kKBlockBytes, &tmD, &ctl->d_full[s], 64 * s, row);
+                } else if (INT8) {
                     if (!mbar_wait(&ctl->i_empty[s], ph ^ 1, abort_flag, p.status, kStatusTimeoutProducer)) break;
                     mbar_arrive_expect_tx(&ctl->i_full[s], kI8TileBytes);
                     tma_load_2d(sI + s * kI8TileBytes, &tmD, &ctl->i_full[s], 0, row);
@@ -219,6 +231,48 @@ maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             // so the 14-bit field never carries.
             const uint64_t a_desc0 = desc_sw128_kmajor(smem_u32(sQ));
             const uint64_t b_desc0 = desc_sw128_kmajor(smem_u32(sD));
+            if (ksplit) {
+                // per tile, M-tile by M-tile: K-block 0 then K-block 1 into
+                // its slot (K in order, the slot handed to the epilogue as
+                // early as before); the K-block-0 half-stage is released
+                // after the last M-tile's K-block 0, so the next tile's first
+                // half loads while the last K-block-1 MMAs run
+                for (int j = 0; ok && j < n_tiles; ++j) {
+                    if (!mbar_wait(&ctl->d_full[0], j & 1, abort_flag, p.status, kStatusTimeoutMma)) break;
+                    tc_fence_after();
+                    for (int mt = 0; mt < n_mt; ++mt) {
+                        const int slot = mt + NMT * (j % (C::kSlots / NMT));
+                        const uint32_t use = j / (C::kSlots / NMT);
+                        if (!mbar_wait(&ctl->t_empty[slot], (use & 1) ^ 1, abort_flag, p.status, kStatusTimeoutMma)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t a_desc = a_desc0 + static_cast<uint64_t>((mt * kTileBytes) >> 4);
+                        const uint32_t d_tmem = tmem_base + slot * kSlotCols;
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; ++k4) {
+                            const uint64_t koff = static_cast<uint64_t>((k4 * 32) >> 4);
+                            mma_f16_ss(d_tmem, a_desc + koff, b_desc0 + koff, p.idesc, k4 > 0 ? 1u : 0u);
+                        }
+                        if (mt == n_mt - 1) mma_commit(&ctl->d_empty[0]);
+                        if (mt == 0) {
+                            if (!mbar_wait(&ctl->d_full[1], j & 1, abort_flag, p.status, kStatusTimeoutMma)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                        }
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; ++k4) {
+                            const uint64_t koff = static_cast<uint64_t>((kKBlockBytes + k4 * 32) >> 4);
+                            mma_f16_ss(d_tmem, a_desc + koff, b_desc0 + koff, p.idesc, 1u);
+                        }
+                        mma_commit(&ctl->t_full[slot]);
+                    }
+                    if (ok) mma_commit(&ctl->d_empty[1]);
+                }
+            } else
             for (int j = 0; ok && j < n_tiles; ++j) {
                 const int s = j % C::kStages;
                 if (!mbar_wait(&ctl->d_full[s], (j / C::kStages) & 1, abort_flag, p.status, kStatusTimeoutMma)) break;

@@ -31,6 +31,7 @@ struct FwdParams {
     int32_t total_tokens;
     int64_t ld_out;         // documents per output row (>= n_docs)
     int32_t groups, parts;  // grid = groups * parts CTAs
+    int32_t ksplit;         // two-M-tile 16-bit launch: stream K-blocks as half-stages
     uint32_t idesc;         // tcgen05 instruction descriptor
     double int8_scale;      // (double)q_scale * (double)d_scale
 };
@@ -39,13 +40,19 @@ struct FwdParams {
 // 16-bit: two CTAs of two M-tiles per SM, except for 257-384 rows, where one
 // CTA of four M-tiles (one of them empty) finishes sooner than two groups of
 // two.  With several row groups every group gets the same share of the SMs,
-// so a part-filled last group of four saves no time.  INT8 keeps four above 256 rows (its two-M-tile form runs one CTA
-// per SM).
+// so a part-filled last group of four saves no time.  INT8 keeps four above
+// 256 rows (its two-M-tile form runs one CTA per SM).
 inline int forward_mtiles(int64_t rows, bool int8) {
     if (rows <= 128) return 1;
     if (rows <= 256) return 2;
     return (int8 || rows <= 384) ? 4 : 2;
 }
+
+// Half-stage (K-block) streaming at two M-tiles: it hides part of the load
+// latency of the single document stage, which pays where loads set the pace
+// (without argmax, or with four or more row groups reading each tile); with
+// the argmax epilogue setting the pace it measured about 1% slower.
+inline bool forward_ksplit(bool with_argmax, int64_t groups) { return !with_argmax || groups >= 4; }
 
 // fwd_tc.cu
 int forward_smem_bytes(int nmt, bool int8);
