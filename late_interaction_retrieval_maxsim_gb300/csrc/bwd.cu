@@ -104,6 +104,26 @@ __global__ void __launch_bounds__(256) csr_chunk_hist_kernel(BwdParams p, bool l
     }
 }
 
+// Per document (one CTA), when the forward left the token counts:
+// doc_count[b] = the sum of the document's chunks * ld counts (a contiguous
+// range of chunk_cnt), in a fixed order.
+__global__ void __launch_bounds__(256) csr_doc_total_kernel(BwdParams p) {
+    const int b = blockIdx.x;
+    const int64_t lo = static_cast<int64_t>(p.chunks) * p.cu_seqlens[b];
+    const int64_t hi = static_cast<int64_t>(p.chunks) * p.cu_seqlens[b + 1];
+    int sum = 0;
+    for (int64_t k = lo + threadIdx.x; k < hi; k += blockDim.x) sum += p.chunk_cnt[k];
+    __shared__ int red[256 / 32];
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = sum;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int s = 0;
+        for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) s += red[w];
+        p.doc_count[b] = s;
+    }
+}
+
 // Per document (one CTA): row_ptr of its tokens, and chunk_cnt[c][t] turned
 // into the first CSR slot of chunk c's sources for token t
 // (row_ptr[t] + the counts of the earlier chunks for t).
@@ -398,6 +418,7 @@ cudaError_t launch_build_csr(const BwdParams &p, cudaStream_t stream, bool count
     }
     // (with counts from the forward, documents too long for the CSR are
     // reported by csr_place_kernel)
+    if (counts_ready) csr_doc_total_kernel<<<p.n_docs, 256, 0, stream>>>(p);
     csr_doc_scan_kernel<<<1, 1024, 0, stream>>>(p);
     csr_token_scan_kernel<<<p.n_docs, 256, 0, stream>>>(p);
     if ((e = cudaFuncSetAttribute(csr_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -308,8 +308,6 @@ __device__ __forceinline__ void epilogue_warp(const FwdParams &p, int rho_warp, 
             if (src)
                 atomicAdd(p.csr_cnt + static_cast<int64_t>(p.csr_chunks) * doc_lo +
                               static_cast<int64_t>(csr_chunk) * ldb + (a - doc_lo), 1);
-            const unsigned bal = __ballot_sync(0xffffffffu, src);
-            if (lane == 0 && bal != 0u) atomicAdd(p.csr_doc_count + b, __popc(bal));
         }
         if (INT8) {
             const bool empty_doc = doc_hi == doc_lo;

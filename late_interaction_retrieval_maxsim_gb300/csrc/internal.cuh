@@ -24,7 +24,6 @@ struct FwdParams {
     const float *q_tok_scale;  // INT8 per-token mode: [n_q, lq_max] query-token scales
     const float *d_tok_scale;  // INT8 per-token mode: [total_tokens] document-token scales
     int32_t *csr_cnt;          // training mode (or null): per-(document, chunk, token) source counts
-    int32_t *csr_doc_count;    // training mode: sources per document
     int32_t csr_chunks, csr_chunk_len;
     int32_t *status;     // device status word
     int32_t n_q, lq_max, lq_pad, n_docs;

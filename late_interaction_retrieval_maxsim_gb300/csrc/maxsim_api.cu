@@ -884,10 +884,10 @@ maxsim_status_t maxsim_forward_with_counts(const void *Q, const int32_t *q_lens,
     if (backward_workspace == nullptr || backward_workspace_bytes < bl.total) return MAXSIM_ERR_WORKSPACE;
 
     uint8_t *bws = static_cast<uint8_t *>(backward_workspace);
-    int32_t *doc_count = reinterpret_cast<int32_t *>(bws + bl.row_ptr + bl.col_idx);
     int32_t *chunk_cnt = reinterpret_cast<int32_t *>(bws + bl.row_ptr + bl.col_idx + bl.doc_count);
-    // the counts start at zero (doc_count and chunk_cnt are adjacent)
-    if (cudaMemsetAsync(doc_count, 0, bl.doc_count + bl.chunk_cnt, stream) != cudaSuccess) return MAXSIM_ERR_CUDA;
+    // the counts start at zero; the per-document totals are summed from them
+    // by the backward
+    if (cudaMemsetAsync(chunk_cnt, 0, bl.chunk_cnt, stream) != cudaSuccess) return MAXSIM_ERR_CUDA;
     ForwardPlan plan;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     st = forward_prepare(plan, Q, q_lens, n_q, lq_max, dtype, 1.0f, 1.0f, ws, ws + wl.partials, stream);
@@ -895,7 +895,6 @@ maxsim_status_t maxsim_forward_with_counts(const void *Q, const int32_t *q_lens,
     const int chunks = csr_chunks(n_q, lq_max, n_docs);
     const int64_t n_cand = static_cast<int64_t>(n_q) * lq_max;
     plan.p.csr_cnt = chunk_cnt;
-    plan.p.csr_doc_count = doc_count;
     plan.p.csr_chunks = chunks;
     plan.p.csr_chunk_len = static_cast<int32_t>(std::max<int64_t>(1, (n_cand + chunks - 1) / chunks));
     return forward_block(plan, D, cu_seqlens, n_docs, total_d_tokens, scores, nullptr, argmax, n_docs, stream);

@@ -50,9 +50,12 @@ def test_autograd_matches_torch_reference(ops, dtype):
     assert torch.allclose(Da.grad.float(), Dr.grad, atol=tol, rtol=0)
 
 
-def test_autograd_grads_equal_the_c_abi_backward(ops):
+@pytest.mark.parametrize("lq", [32, 100])
+def test_autograd_grads_equal_the_c_abi_backward(ops, lq):
+    """Bit-equal to the C ABI's forward + backward: with the counting pair
+    (32-token queries) and with the plain pair (100-token queries)."""
     from late_interaction_retrieval_maxsim_gb300.autograd import maxsim
-    Q, ql, D, cu = random_case(4, 32, [180] * 16, "bf16", seed=78)
+    Q, ql, D, cu = random_case(4, lq, [180] * 16, "bf16", seed=78)
     Qa = Q.clone().requires_grad_(True)
     Da = D.clone().requires_grad_(True)
     s = maxsim(Qa, Da, ql, cu)
