@@ -161,61 +161,106 @@ __device__ __forceinline__ void split8(const uint32_t (&r)[32], int o, float &be
     above = fmax3(fmax3(y[0], y[1], y[2]), fmax3(y[3], y[4], y[5]), fmaxf(y[6], y[7]));
 }
 
-// Maxima of columns [0, p) and [p, 32) for a document boundary at p
-// (1 <= p <= 31): eight-column group maxima, with only the group holding the
-// boundary masked column by column.
-__device__ __forceinline__ void split_max32(const uint32_t (&r)[32], int p, float &left, float &right) {
-    const float g0 = max8<0>(r), g1 = max8<8>(r), g2 = max8<16>(r), g3 = max8<24>(r);
-    const int o = p & 7;
+// Maxima of columns [0, p) and [p, 32) for a document boundary at p = 8G + o
+// (1 <= p <= 31): eight-column group maxima, with only group G, the one
+// holding the boundary, masked column by column.
+template <int G>
+__device__ __forceinline__ void split_max32(const uint32_t (&r)[32], int o, float &left, float &right) {
     float lo, hi;
-    switch (p >> 3) {
-        case 0:
-            split8<0>(r, o, lo, hi);
-            left = lo;
-            right = fmax3(hi, g1, fmaxf(g2, g3));
-            break;
-        case 1:
-            split8<8>(r, o, lo, hi);
-            left = fmaxf(g0, lo);
-            right = fmax3(hi, g2, g3);
-            break;
-        case 2:
-            split8<16>(r, o, lo, hi);
-            left = fmax3(g0, g1, lo);
-            right = fmaxf(hi, g3);
-            break;
-        default:
-            split8<24>(r, o, lo, hi);
-            left = fmax3(g0, g1, fmaxf(g2, lo));
-            right = hi;
-            break;
+    split8<8 * G>(r, o, lo, hi);
+    if constexpr (G == 0) {
+        left = lo;
+        right = fmax3(hi, max8<8>(r), fmaxf(max8<16>(r), max8<24>(r)));
+    } else if constexpr (G == 1) {
+        left = fmaxf(max8<0>(r), lo);
+        right = fmax3(hi, max8<16>(r), max8<24>(r));
+    } else if constexpr (G == 2) {
+        left = fmax3(max8<0>(r), max8<8>(r), lo);
+        right = fmaxf(hi, max8<24>(r));
+    } else {
+        left = fmax3(max8<0>(r), max8<8>(r), fmaxf(max8<16>(r), lo));
+        right = hi;
     }
 }
 
-// A chunk in which the current document ends at column p (1 <= p <= 31) and
-// the next one covers the rest: [0, p) is folded into (m, a); the next
+// below_mask32 against two maxima at once: bit k set when column k holds a
+// value below its own segment's maximum -- tl for k < 8G + o, tr from there
+// on -- so one pass serves the ending document's search and the next one's.
+// Only the eight columns of group G choose their target at run time.
+template <int G>
+__device__ __forceinline__ uint32_t below_mask32_split(const uint32_t (&r)[32], int o, float tl, float tr,
+                                                       bool fast) {
+    auto left_of = [&](int k) -> bool {
+        if (k < 8 * G) return true;
+        if (k >= 8 * G + 8) return false;
+        return k - 8 * G < o;
+    };
+    float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    if (fast) {
+        const float S = 0x1p100f;
+        const float Cl = tl * S, Cr = tr * S;
+#pragma unroll
+        for (int g = 0; g < 2; ++g)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int k0 = 16 * g + j, k1 = 16 * g + 8 + j;
+                const float w = static_cast<float>(1u << j);
+                const float2 ind = make_float2(fma_sat(__uint_as_float(r[k0]), -S, left_of(k0) ? Cl : Cr),
+                                               fma_sat(__uint_as_float(r[k1]), -S, left_of(k1) ? Cl : Cr));
+                acc[g] = fma2(ind, make_float2(w, w), acc[g]);
+            }
+    } else {
+#pragma unroll
+        for (int g = 0; g < 2; ++g)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int k0 = 16 * g + j, k1 = 16 * g + 8 + j;
+                const float w = static_cast<float>(1u << j);
+                const float t0 = (left_of(k0) ? tl : tr) - __uint_as_float(r[k0]);
+                const float t1 = (left_of(k1) ? tl : tr) - __uint_as_float(r[k1]);
+                const float2 ind = make_float2(mul_sat(mul_sat(t0, 0x1p127f), 0x1p23f),
+                                               mul_sat(mul_sat(t1, 0x1p127f), 0x1p23f));
+                acc[g] = fma2(ind, make_float2(w, w), acc[g]);
+            }
+    }
+    const float lo = fmaf(acc[0].y, 256.f, acc[0].x);
+    const float hi = fmaf(acc[1].y, 256.f, acc[1].x);
+    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+// A chunk in which the current document ends at column p = 8G + o and the
+// next one covers the rest: [0, p) is folded into (m, a); the next
 // document's running state starts as (m_next, a_next) from [p, 32).
+template <bool ARGMAX, int G>
+__device__ __forceinline__ void fold_split_g(const uint32_t (&r)[32], int c0, int o, float &m, int &a,
+                                             float &m_next, int &a_next) {
+    float left, right;
+    split_max32<G>(r, o, left, right);
+    m_next = right;
+    if (!ARGMAX) {
+        m = fmaxf(m, left);
+        return;
+    }
+    const int p = 8 * G + o;
+    const uint32_t low = (1u << p) - 1u;
+    const bool fast = __all_sync(0xffffffffu, fast_indicator_ok(right) && fast_indicator_ok(left));
+    const uint32_t mask = below_mask32_split<G>(r, o, left, right, fast);
+    a_next = c0 + __ffs(~(mask | low)) - 1;
+    if (left > m) {
+        m = left;
+        a = c0 + __ffs(~(mask | ~low)) - 1;
+    }
+}
+
 template <bool ARGMAX>
 __device__ __forceinline__ void fold_split(const uint32_t (&r)[32], int c0, int p, float &m, int &a,
                                            float &m_next, int &a_next) {
-    float left, right;
-    split_max32(r, p, left, right);
-    if (!ARGMAX) {
-        m = fmaxf(m, left);
-        m_next = right;
-        return;
-    }
-    const bool up = left > m;
-    const uint32_t low = (1u << p) - 1u;
-    const bool fast = __all_sync(0xffffffffu, fast_indicator_ok(right) && (!up || fast_indicator_ok(left)));
-    m_next = right;
-    a_next = c0 + __ffs(~(below_mask32(r, right, fast) | low)) - 1;
-    if (__any_sync(0xffffffffu, up)) {
-        const uint32_t mask = below_mask32(r, left, fast) | ~low;
-        if (up) {
-            m = left;
-            a = c0 + __ffs(~mask) - 1;
-        }
+    const int o = p & 7;
+    switch (p >> 3) {
+        case 0: fold_split_g<ARGMAX, 0>(r, c0, o, m, a, m_next, a_next); break;
+        case 1: fold_split_g<ARGMAX, 1>(r, c0, o, m, a, m_next, a_next); break;
+        case 2: fold_split_g<ARGMAX, 2>(r, c0, o, m, a, m_next, a_next); break;
+        default: fold_split_g<ARGMAX, 3>(r, c0, o, m, a, m_next, a_next); break;
     }
 }
 

@@ -9,13 +9,17 @@
 // token).
 //
 // GB300 design (differs from the pages' one-program-per-pair scheme):
-//  * One CTA owns up to 4 M-tiles of 128 padded query rows (all queries of a
-//    small batch at once) resident in shared memory, and streams a
-//    token-balanced contiguous range of documents through a TMA pipeline, so
-//    every document row is read from HBM once for all those queries.
+//  * One CTA owns 1, 2 or 4 M-tiles of 128 padded query rows resident in
+//    shared memory, and streams a token-balanced contiguous range of
+//    documents through a TMA pipeline, so every document row is read from
+//    HBM once for all those queries (further row groups re-read it from L2).
+//    With 1 or 2 M-tiles two CTAs share an SM, each with half of TMEM and of
+//    shared memory; at 2 M-tiles the single document stage may be streamed
+//    one K-block half at a time so the next tile's first half loads while
+//    the last MMAs of the current one run.
 //  * tcgen05.mma (M=128, N=128 tokens, K=16, FP32 accumulate) writes
-//    similarity tiles into TMEM; 4 accumulator slots of 128 columns let the
-//    MMA run ahead of the epilogue.
+//    similarity tiles into TMEM accumulator slots of 128 columns (4 per SM),
+//    which the MMA fills while the epilogue drains the others.
 //  * Epilogue warps (one warp-set of 4 per M-tile, one thread per query row)
 //    read TMEM with tcgen05.ld and fold each 32-column chunk into the row's
 //    running (max, argmax) with a balanced comparison tree (ties keep the
