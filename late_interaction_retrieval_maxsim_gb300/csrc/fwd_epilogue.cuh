@@ -63,6 +63,12 @@ __device__ __forceinline__ bool fast_indicator_ok(float cm) {
     return x >= 0x1p-77f && x < 0x1p27f;
 }
 
+// The 32-bit mask from its two 16-bit halves, each held as the float
+// 2^23 + half (so its low 16 mantissa bits are the half): one byte permute.
+__device__ __forceinline__ uint32_t mask_from_halves(float lo, float hi) {
+    return __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x5410);
+}
+
 // Bit k set when column k holds a value below cm, clear when it equals cm
 // (columns above cm, which only occur outside a segment, come out clear and
 // must be masked by the caller).
@@ -78,8 +84,10 @@ __device__ __forceinline__ bool fast_indicator_ok(float cm) {
 // of distinct powers of two below 2^16 are exact in FP32).
 __device__ __forceinline__ uint32_t below_mask32(const uint32_t (&r)[32], float cm, bool fast) {
     // acc[g] accumulates columns (16g + j, 16g + 8 + j), j = 0..7, with weight 2^j
-    // in its x / y lane: two indicators per packed FMA.
-    float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    // in its x / y lane: two indicators per packed FMA.  The x lanes start at
+    // 2^23, so each combined 16-bit half is read straight out of a float's
+    // mantissa (2^23 + n, n < 2^16, is exact).
+    float2 acc[2] = {make_float2(0x1p23f, 0.f), make_float2(0x1p23f, 0.f)};
     if (fast) {
         const float S = 0x1p100f;
         const float C = cm * S;
@@ -106,9 +114,7 @@ __device__ __forceinline__ uint32_t below_mask32(const uint32_t (&r)[32], float 
             }
     }
     // bits 0-7 / 8-15 of each half from the x / y lanes
-    const float lo = fmaf(acc[0].y, 256.f, acc[0].x);
-    const float hi = fmaf(acc[1].y, 256.f, acc[1].x);
-    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+    return mask_from_halves(fmaf(acc[0].y, 256.f, acc[0].x), fmaf(acc[1].y, 256.f, acc[1].x));
 }
 
 // Bits lo .. hi-1 set (0 <= lo < hi <= 32).
@@ -195,7 +201,8 @@ __device__ __forceinline__ uint32_t below_mask32_split(const uint32_t (&r)[32], 
         if (k >= 8 * G + 8) return false;
         return k - 8 * G < o;
     };
-    float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    // x lanes start at 2^23 (see below_mask32)
+    float2 acc[2] = {make_float2(0x1p23f, 0.f), make_float2(0x1p23f, 0.f)};
     if (fast) {
         const float S = 0x1p100f;
         const float Cl = tl * S, Cr = tr * S;
@@ -223,9 +230,7 @@ __device__ __forceinline__ uint32_t below_mask32_split(const uint32_t (&r)[32], 
                 acc[g] = fma2(ind, make_float2(w, w), acc[g]);
             }
     }
-    const float lo = fmaf(acc[0].y, 256.f, acc[0].x);
-    const float hi = fmaf(acc[1].y, 256.f, acc[1].x);
-    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+    return mask_from_halves(fmaf(acc[0].y, 256.f, acc[0].x), fmaf(acc[1].y, 256.f, acc[1].x));
 }
 
 // A chunk in which the current document ends at column p = 8G + o and the
