@@ -189,8 +189,11 @@ def _extra_workloads(m, syn, rl, peaks):
     import torch
     out = {}
     stream = torch.cuda.current_stream()
-    for name in ("colbert_1q", "colpali", "train", "train_colpali", "int8_varlen"):
+    for name in ("colbert_varlen", "colbert_1q", "colpali", "train", "train_colpali", "int8_varlen"):
         w = syn.WORKLOADS[name]
+        torch.cuda.empty_cache()
+        torch.cuda.reset_peak_memory_stats()
+        base_bytes = torch.cuda.memory_allocated()   # what earlier lines still hold
         x = syn.make_inputs(w, device="cuda")
         Q, ql, D, cu = x["Q"], x["q_lens"], x["D"], x["cu_seqlens"]
         kw = dict(q_scale=x["q_scale"], d_scale=x["d_scale"])
@@ -200,11 +203,20 @@ def _extra_workloads(m, syn, rl, peaks):
         _, per = _time_loop(lambda: m.maxsim_forward(Q, ql, D, cu, scores=s, argmax=a, workspace=ws,
                                                      **kw), 20, 3, stream)
         ms = statistics.median(per)
+        # device memory held by one forward: inputs, outputs and workspace
+        # (the similarity tensor is never materialised; its FP32 size for
+        # comparison)
+        peak_bytes = torch.cuda.max_memory_allocated() - base_bytes
+        _, per_v = _time_loop(lambda: m.maxsim_forward(Q, ql, D, cu, with_argmax=False, scores=s, workspace=ws,
+                                                       **kw), 20, 3, stream)
         flops = rl.forward_flops(int(ql.sum()), D.shape[0])
         rec = {"n_q": w.n_q, "lq": w.lq, "n_docs": w.n_docs, "ld": [w.ld_lo, w.ld_hi],
                "dtype": w.dtype, "fwd_ms": round(ms, 4), "docs_per_s": w.n_docs / (ms / 1e3),
                "fwd_tflops": flops / (ms / 1e3) / 1e12,
-               "fwd_frac_of_measured_bf16_peak": flops / (ms / 1e3) / 1e12 / peaks["bf16_tflops"]}
+               "fwd_frac_of_measured_bf16_peak": flops / (ms / 1e3) / 1e12 / peaks["bf16_tflops"],
+               "fwd_value_only_ms": round(statistics.median(per_v), 4),
+               "peak_device_bytes": int(peak_bytes),
+               "similarity_tensor_fp32_bytes": int(ql.sum()) * D.shape[0] * 4}
         if name == "colbert_1q":
             # one query: 32 FLOP per document byte, far below the ridge -- HBM-bound
             hb = rl.forward_hbm_bytes(w.n_q, w.lq, w.n_docs, D.shape[0])
@@ -246,6 +258,7 @@ def _extra_workloads(m, syn, rl, peaks):
             rec["device_status"] = "fault"
         out[name] = rec
         del x, Q, D, s, a
+        ws = cu = ql = g = bws = dq = dd = None
         torch.cuda.empty_cache()
     out["out_of_core_colpali"] = _out_of_core(m, syn)
     out.update(_int8_variants(m, syn))

@@ -446,6 +446,18 @@ maxsim_status_t maxsim_backward_with_counts(const float *grad_scores, const int3
  */
 maxsim_status_t maxsim_device_status(void *stream, int32_t clear, int32_t *code);
 
+/*
+ * Self-test of the kernels' failure path (no fault is involved): enqueues on
+ * `stream` one CTA that holds tensor memory and waits on a barrier nothing
+ * completes.  Its bounded wait gives up after `limit_us` microseconds
+ * (1 .. 1,000,000), raises the CTA's abort flag (a second waiter returns on
+ * it), records 0x105 in the device status word, releases the tensor memory
+ * and exits.  Afterwards maxsim_device_status reports 0x105 and every entry
+ * point works as before.  Returns MAXSIM_ERR_INVALID_ARGUMENT for a limit
+ * out of range, MAXSIM_ERR_CUDA on a launch failure, else MAXSIM_OK.
+ */
+maxsim_status_t maxsim_selftest_bounded_wait(uint32_t limit_us, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

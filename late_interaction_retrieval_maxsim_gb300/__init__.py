@@ -37,7 +37,7 @@ __all__ = [
     "maxsim_forward_host_workspace_size", "maxsim_forward_int8_per_token", "maxsim_topk",
     "maxsim_rerank_two_stage", "maxsim_rerank_workspace_size", "maxsim_chamfer_forward",
     "maxsim_chamfer_backward", "maxsim_chamfer_build_csr", "maxsim_forward_with_counts",
-    "maxsim_backward_with_counts", "MaxSimError", "DTYPE_CODES",
+    "maxsim_backward_with_counts", "maxsim_selftest_bounded_wait", "MaxSimError", "DTYPE_CODES",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -122,6 +122,8 @@ def load_library():
     lib.maxsim_backward_with_counts.restype = ctypes.c_int
     lib.maxsim_device_status.argtypes = [vp, i32, ctypes.POINTER(i32)]
     lib.maxsim_device_status.restype = ctypes.c_int
+    lib.maxsim_selftest_bounded_wait.argtypes = [ctypes.c_uint32, vp]
+    lib.maxsim_selftest_bounded_wait.restype = ctypes.c_int
     _LIB = lib
     return lib
 
@@ -639,6 +641,14 @@ def maxsim_backward_with_counts(grad_scores, argmax, Q, q_lens, D, cu_seqlens, b
                                              backward_workspace.numel(), _stream(stream))
     _check("maxsim_backward_with_counts", st)
     return dQ, dD
+
+
+def maxsim_selftest_bounded_wait(limit_us: int = 5000, stream=None) -> None:
+    """C: ``maxsim_selftest_bounded_wait`` -- enqueue the bounded-wait
+    self-test (one CTA whose wait gives up after ``limit_us`` microseconds and
+    records 0x105 in the device status word)."""
+    lib = load_library()
+    _check("maxsim_selftest_bounded_wait", lib.maxsim_selftest_bounded_wait(int(limit_us), _stream(stream)))
 
 
 def maxsim_device_status(clear: bool = True, stream=None) -> int:

@@ -489,6 +489,43 @@ cudaError_t launch_rebase_offsets(const int32_t *src, int32_t *dst, int32_t n, c
     return cudaGetLastError();
 }
 
+// The forward's failure path in miniature: warp 1 holds TMEM, thread 0 waits
+// on a barrier that nothing completes until its bounded wait gives up
+// (raising the CTA's abort flag and recording the status code), thread 32
+// waits on the same barrier until it sees the abort flag; then the CTA
+// releases TMEM and exits as the forward does.
+__global__ void __launch_bounds__(64) wait_selftest_kernel(int32_t *status, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ uint32_t tmem_base;
+    __shared__ int32_t abort_word;
+    volatile int32_t *abort_flag = &abort_word;
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        abort_word = 0;
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_base, 32);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (threadIdx.x == 0) mbar_wait(&bar, 0, abort_flag, status, kStatusSelfTestExpired, limit_ns);
+    if (threadIdx.x == 32) mbar_wait(&bar, 0, abort_flag, status, kStatusSelfTestExpired, 4 * limit_ns);
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, 32);
+}
+
+cudaError_t launch_wait_selftest(int32_t *status, uint64_t limit_ns, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 64, 0, stream>>>(status, limit_ns);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_int8_to_f16(const int8_t *src, uint16_t *dst, int64_t n, cudaStream_t stream) {
     if (n == 0) return cudaSuccess;
     int8_to_f16_kernel<<<grid_for(n, 256), 256, 0, stream>>>(src, reinterpret_cast<__half *>(dst), n);

@@ -68,6 +68,9 @@ cudaError_t launch_finalize_partials(const FwdParams &p, bool int8, cudaStream_t
 cudaError_t launch_fill_empty(const FwdParams &p, bool int8, cudaStream_t stream);
 cudaError_t launch_int8_to_f16(const int8_t *src, uint16_t *dst, int64_t n, cudaStream_t stream);
 cudaError_t launch_rebase_offsets(const int32_t *src, int32_t *dst, int32_t n, cudaStream_t stream);
+// One CTA holding TMEM waits on an mbarrier that nothing completes: the
+// bounded wait must give up after limit_ns and record kStatusSelfTestExpired.
+cudaError_t launch_wait_selftest(int32_t *status, uint64_t limit_ns, cudaStream_t stream);
 
 // topk.cu
 constexpr int kTopkMax = 4096;  // largest k a row-wise top-K selection takes

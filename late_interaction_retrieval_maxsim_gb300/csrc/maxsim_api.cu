@@ -909,6 +909,15 @@ maxsim_status_t maxsim_backward_with_counts(const float *grad_scores, const int3
                          dtype, dQ, dD, workspace, workspace_bytes, static_cast<cudaStream_t>(stream_), true);
 }
 
+maxsim_status_t maxsim_selftest_bounded_wait(uint32_t limit_us, void *stream_) {
+    if (limit_us == 0 || limit_us > 1000000u) return MAXSIM_ERR_INVALID_ARGUMENT;
+    DeviceInfo di;
+    maxsim_status_t st = device_info(&di);
+    if (st != MAXSIM_OK) return st;
+    return cuda_status(launch_wait_selftest(di.status, static_cast<uint64_t>(limit_us) * 1000u,
+                                            static_cast<cudaStream_t>(stream_)));
+}
+
 maxsim_status_t maxsim_device_status(void *stream_, int32_t clear, int32_t *code) {
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     int32_t v = 0;

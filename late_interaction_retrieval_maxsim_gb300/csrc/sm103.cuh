@@ -20,6 +20,7 @@ enum : int32_t {
     kStatusTimeoutMma = 0x102,
     kStatusTimeoutEpilogue = 0x103,
     kStatusTimeoutDrain = 0x104,
+    kStatusSelfTestExpired = 0x105,   // the bounded-wait self-test's expected code
     kStatusBadArgmax = 0x201,
     kStatusDocTooLong = 0x202,
     kStatusSetTooLarge = 0x203,
@@ -87,16 +88,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity, ui
 
 // Wait for the phase of `bar` with the given parity, sleeping in the
 // barrier between probes.  Gives up (returns false) when *abort becomes
-// non-zero or after kWaitLimitNs; on a timeout it raises *abort and records
+// non-zero or after limit_ns (default kWaitLimitNs); on a timeout it raises *abort and records
 // `code` in *status.  `abort` may be null (then only the time limit applies).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int32_t *abort,
-                                          int32_t *status, int32_t code) {
+                                          int32_t *status, int32_t code, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_test(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     while (true) {
         if (mbar_try_wait(bar, parity, 200000u)) return true;
         if (abort != nullptr && *abort != 0) return false;
-        if (globaltimer() - t0 > kWaitLimitNs) {
+        if (globaltimer() - t0 > limit_ns) {
             if (abort != nullptr) *abort = 1;
             atomicCAS(status, 0, code);
             return false;

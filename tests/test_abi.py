@@ -55,6 +55,10 @@ def test_workspace_sizes(lib):
 
 def test_argument_errors_return_before_touching_the_device(lib):
     vp = ctypes.c_void_p
+    # bounded-wait self-test: limit out of range -> invalid argument
+    lib.maxsim_selftest_bounded_wait.argtypes = [ctypes.c_uint32, vp]
+    assert lib.maxsim_selftest_bounded_wait(0, None) == 1
+    assert lib.maxsim_selftest_bounded_wait(1_000_001, None) == 1
     # dim != 128 -> unsupported; bad dtype -> unsupported
     f = lib.maxsim_forward
     assert f(vp(16), vp(16), 1, 32, vp(16), vp(16), 1, 10, 64, 0, 1.0, 1.0,
