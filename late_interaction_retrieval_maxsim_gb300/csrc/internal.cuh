@@ -48,10 +48,14 @@ inline int forward_mtiles(int64_t rows, bool int8) {
 }
 
 // Half-stage (K-block) streaming at two M-tiles: it hides part of the load
-// latency of the single document stage, which pays where loads set the pace
-// (without argmax, or with four or more row groups reading each tile); with
-// the argmax epilogue setting the pace it measured about 1% slower.
-inline bool forward_ksplit(bool with_argmax, int64_t groups) { return !with_argmax || groups >= 4; }
+// latency of the single document stage, which pays where loads set the pace:
+// without argmax, or with long documents (few boundaries, rare argmax
+// searches: 1024-token pages 2.19 -> 2.11 ms).  Where the argmax epilogue sets
+// the pace (documents of a few hundred tokens) it gains nothing and costs up
+// to 2% (256 x 32 queries vs 180-token documents).
+inline bool forward_ksplit(bool with_argmax, int64_t total_tokens, int64_t n_docs) {
+    return !with_argmax || total_tokens >= 512 * n_docs;
+}
 
 // fwd_tc.cu
 int forward_smem_bytes(int nmt, bool int8);

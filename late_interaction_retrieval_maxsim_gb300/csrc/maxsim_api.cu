@@ -318,7 +318,7 @@ maxsim_status_t forward_block(ForwardPlan &plan, const void *D, const int32_t *c
     if (groups * parts > INT32_MAX) return MAXSIM_ERR_INVALID_ARGUMENT;
     p.groups = static_cast<int32_t>(groups);
     p.parts = static_cast<int32_t>(parts);
-    p.ksplit = forward_ksplit(argmax != nullptr, groups) ? 1 : 0;
+    p.ksplit = forward_ksplit(argmax != nullptr, total, n_docs) ? 1 : 0;
     cudaError_t e = launch_forward(plan.tmQ, tmD, p, plan.nmt, argmax != nullptr, plan.mode, stream);
     if (e != cudaSuccess) return MAXSIM_ERR_CUDA;
     if (p.lq_pad > 32) return cuda_status(launch_finalize_partials(p, int64_sums, stream));
