@@ -192,9 +192,9 @@ def _extra_workloads(m, syn, rl, peaks):
     for name in ("colbert_varlen", "colbert_1q", "colpali", "train", "train_colpali", "int8_varlen"):
         w = syn.WORKLOADS[name]
         torch.cuda.empty_cache()
-        torch.cuda.reset_peak_memory_stats()
         base_bytes = torch.cuda.memory_allocated()   # what earlier lines still hold
         x = syn.make_inputs(w, device="cuda")
+        torch.cuda.reset_peak_memory_stats()         # not the generator's temporaries
         Q, ql, D, cu = x["Q"], x["q_lens"], x["D"], x["cu_seqlens"]
         kw = dict(q_scale=x["q_scale"], d_scale=x["d_scale"])
         s, a, _ = m.maxsim_forward(Q, ql, D, cu, **kw)

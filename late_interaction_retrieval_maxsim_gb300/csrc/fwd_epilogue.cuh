@@ -483,7 +483,7 @@ __device__ __forceinline__ void epilogue_warp(const FwdParams &p, int rho_warp, 
                 }
             }
         } else {
-            // registers are scarce at 4 M-tiles: one chunk at a time
+            // registers are scarce with 18-20 warps per SM: one chunk at a time
 #pragma unroll 1
             for (int kc = 0; kc < 4; ++kc) {
                 [[maybe_unused]] const float sc = chunk_scale(tile0 + 32 * kc);
