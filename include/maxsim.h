@@ -447,6 +447,22 @@ maxsim_status_t maxsim_backward_with_counts(const float *grad_scores, const int3
 maxsim_status_t maxsim_device_status(void *stream, int32_t clear, int32_t *code);
 
 /*
+ * The launch layout maxsim_forward (and maxsim_forward_int8_per_token, with
+ * dtype MAXSIM_INT8) would use for these sizes, computed on the host without
+ * touching a device; `sm_count` is the device's SM count (152 on a GB300).
+ * Writes five int32 into `layout`: M-tiles of 128 padded query rows per CTA
+ * (1, 2 or 4), CTAs per SM, row groups, CTAs (token-balanced document parts)
+ * per row group, and 1 when the single document stage streams as two K-block
+ * halves.  All five are 0 when no forward kernel would launch (no query, no
+ * document, lq_max 0 or no document token).  Returns MAXSIM_ERR_UNSUPPORTED
+ * for an unknown dtype, MAXSIM_ERR_INVALID_ARGUMENT for a null `layout`,
+ * negative sizes, sm_count <= 0 or sizes beyond the forward's limits.
+ */
+maxsim_status_t maxsim_forward_plan(int32_t n_q, int32_t lq_max, int32_t n_docs, int64_t total_d_tokens,
+                                    maxsim_dtype_t dtype, int32_t with_argmax, int32_t sm_count,
+                                    int32_t *layout);
+
+/*
  * Self-test of the kernels' failure path (no fault is involved): enqueues on
  * `stream` one CTA that holds tensor memory and waits on a barrier nothing
  * completes.  Its bounded wait gives up after `limit_us` microseconds

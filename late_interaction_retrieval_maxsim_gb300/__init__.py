@@ -37,7 +37,8 @@ __all__ = [
     "maxsim_forward_host_workspace_size", "maxsim_forward_int8_per_token", "maxsim_topk",
     "maxsim_rerank_two_stage", "maxsim_rerank_workspace_size", "maxsim_chamfer_forward",
     "maxsim_chamfer_backward", "maxsim_chamfer_build_csr", "maxsim_forward_with_counts",
-    "maxsim_backward_with_counts", "maxsim_selftest_bounded_wait", "MaxSimError", "DTYPE_CODES",
+    "maxsim_backward_with_counts", "maxsim_selftest_bounded_wait", "maxsim_forward_plan", "MaxSimError",
+    "DTYPE_CODES",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -124,6 +125,8 @@ def load_library():
     lib.maxsim_device_status.restype = ctypes.c_int
     lib.maxsim_selftest_bounded_wait.argtypes = [ctypes.c_uint32, vp]
     lib.maxsim_selftest_bounded_wait.restype = ctypes.c_int
+    lib.maxsim_forward_plan.argtypes = [i32, i32, i32, i64, ctypes.c_int, i32, i32, ctypes.POINTER(i32)]
+    lib.maxsim_forward_plan.restype = ctypes.c_int
     _LIB = lib
     return lib
 
@@ -641,6 +644,26 @@ def maxsim_backward_with_counts(grad_scores, argmax, Q, q_lens, D, cu_seqlens, b
                                              backward_workspace.numel(), _stream(stream))
     _check("maxsim_backward_with_counts", st)
     return dQ, dD
+
+
+def maxsim_forward_plan(n_q: int, lq_max: int, n_docs: int, total_d_tokens: int, dtype="fp16", *,
+                        with_argmax: bool = True, sm_count: int | None = None) -> dict:
+    """C: ``maxsim_forward_plan`` -- the forward's launch layout for these
+    sizes (host only).  ``dtype`` is "fp16", "bf16" or "int8" (or a torch
+    dtype); ``sm_count`` defaults to the current CUDA device's."""
+    lib = load_library()
+    if sm_count is None:
+        torch = _torch()
+        sm_count = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    if not isinstance(dtype, str):
+        torch = _torch()
+        dtype = {torch.float16: "fp16", torch.bfloat16: "bf16", torch.int8: "int8"}[dtype]
+    code = DTYPE_CODES[dtype]
+    out = (ctypes.c_int32 * 5)()
+    _check("maxsim_forward_plan", lib.maxsim_forward_plan(int(n_q), int(lq_max), int(n_docs), int(total_d_tokens),
+                                                          code, 1 if with_argmax else 0, int(sm_count), out))
+    return {"m_tiles": out[0], "ctas_per_sm": out[1], "row_groups": out[2], "parts": out[3],
+            "k_block_halves": bool(out[4])}
 
 
 def maxsim_selftest_bounded_wait(limit_us: int = 5000, stream=None) -> None:

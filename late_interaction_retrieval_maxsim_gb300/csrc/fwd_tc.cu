@@ -440,6 +440,11 @@ int forward_ctas_per_sm(int nmt, bool int8) {
     return nmt == 1 ? Cfg<1, false>::kCtasPerSm : nmt == 2 ? Cfg<2, false>::kCtasPerSm : Cfg<4, false>::kCtasPerSm;
 }
 
+bool forward_stage_split(int nmt, bool int8) {
+    if (int8) return nmt == 1 ? Cfg<1, true>::kKSplit : nmt == 2 ? Cfg<2, true>::kKSplit : Cfg<4, true>::kKSplit;
+    return nmt == 1 ? Cfg<1, false>::kKSplit : nmt == 2 ? Cfg<2, false>::kKSplit : Cfg<4, false>::kKSplit;
+}
+
 int forward_threads(int nmt, bool int8) {
     if (int8) return nmt == 1 ? Cfg<1, true>::kThreads : nmt == 2 ? Cfg<2, true>::kThreads : Cfg<4, true>::kThreads;
     return nmt == 1 ? Cfg<1, false>::kThreads : nmt == 2 ? Cfg<2, false>::kThreads : Cfg<4, false>::kThreads;

@@ -60,6 +60,7 @@ inline bool forward_ksplit(bool with_argmax, int64_t total_tokens, int64_t n_doc
 // fwd_tc.cu
 int forward_smem_bytes(int nmt, bool int8);
 int forward_threads(int nmt, bool int8);
+bool forward_stage_split(int nmt, bool int8);  // the configuration can stream K-block halves
 int forward_ctas_per_sm(int nmt, bool int8);   // CTAs one SM runs at once
 // Forward arithmetic: FP16/BF16 MMA on the inputs; INT8 with one scale per
 // tensor (exact integer maxima, int64 sums); INT8 with one scale per token

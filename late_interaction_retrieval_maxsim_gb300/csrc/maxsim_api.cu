@@ -233,6 +233,27 @@ maxsim_status_t check_forward_args(const void *Q, const int32_t *q_lens, int32_t
     return MAXSIM_OK;
 }
 
+// Grid of one forward launch: row groups of nmt * 128 padded rows, each
+// group's documents split into token-balanced parts (one CTA per group and
+// part, enough parts to fill ctas_per_sm CTAs on every SM), and whether the
+// single document stage streams as K-block halves.
+struct LaunchLayout {
+    int nmt = 0, ctas_per_sm = 0;
+    int64_t groups = 0, parts = 0;
+    bool ksplit = false;
+};
+
+LaunchLayout launch_layout(int64_t rows, int nmt, bool int8, int sm_count, bool with_argmax, int64_t total,
+                           int64_t n_docs) {
+    LaunchLayout l;
+    l.nmt = nmt;
+    l.ctas_per_sm = forward_ctas_per_sm(nmt, int8);
+    l.groups = (rows + nmt * 128 - 1) / (nmt * 128);
+    l.parts = std::max<int64_t>(1, static_cast<int64_t>(l.ctas_per_sm) * sm_count / l.groups);
+    l.ksplit = forward_stage_split(nmt, int8) && forward_ksplit(with_argmax, total, n_docs);
+    return l;
+}
+
 // What a forward over any set of documents shares: the query side (its
 // tensor map, the FP16 widening of an INT8 Q), the tile configuration and
 // the partial-sum scratch.
@@ -309,16 +330,12 @@ maxsim_status_t forward_block(ForwardPlan &plan, const void *D, const int32_t *c
     alignas(64) CUtensorMap tmD;
     maxsim_status_t st = encode_d(&tmD, D, total, plan.dtype, 128u);
     if (st != MAXSIM_OK) return st;
-    // Row groups of nmt * 128 padded rows; each group's documents are split
-    // into token-balanced parts, one CTA per (group, part).
-    const int64_t rows = static_cast<int64_t>(p.n_q) * p.lq_pad;
-    const int64_t groups = (rows + plan.nmt * 128 - 1) / (plan.nmt * 128);
-    const int64_t parts =
-        std::max<int64_t>(1, static_cast<int64_t>(forward_ctas_per_sm(plan.nmt, plan.int8)) * plan.sm_count / groups);
-    if (groups * parts > INT32_MAX) return MAXSIM_ERR_INVALID_ARGUMENT;
-    p.groups = static_cast<int32_t>(groups);
-    p.parts = static_cast<int32_t>(parts);
-    p.ksplit = forward_ksplit(argmax != nullptr, total, n_docs) ? 1 : 0;
+    const LaunchLayout l = launch_layout(static_cast<int64_t>(p.n_q) * p.lq_pad, plan.nmt, plan.int8,
+                                         plan.sm_count, argmax != nullptr, total, n_docs);
+    if (l.groups * l.parts > INT32_MAX) return MAXSIM_ERR_INVALID_ARGUMENT;
+    p.groups = static_cast<int32_t>(l.groups);
+    p.parts = static_cast<int32_t>(l.parts);
+    p.ksplit = l.ksplit ? 1 : 0;
     cudaError_t e = launch_forward(plan.tmQ, tmD, p, plan.nmt, argmax != nullptr, plan.mode, stream);
     if (e != cudaSuccess) return MAXSIM_ERR_CUDA;
     if (p.lq_pad > 32) return cuda_status(launch_finalize_partials(p, int64_sums, stream));
@@ -907,6 +924,28 @@ maxsim_status_t maxsim_backward_with_counts(const float *grad_scores, const int3
                                             void *workspace, size_t workspace_bytes, void *stream_) {
     return backward_impl(grad_scores, argmax, Q, q_lens, n_q, lq_max, D, cu_seqlens, n_docs, total_d_tokens, dim,
                          dtype, dQ, dD, workspace, workspace_bytes, static_cast<cudaStream_t>(stream_), true);
+}
+
+maxsim_status_t maxsim_forward_plan(int32_t n_q, int32_t lq_max, int32_t n_docs, int64_t total_d_tokens,
+                                    maxsim_dtype_t dtype, int32_t with_argmax, int32_t sm_count,
+                                    int32_t *layout) {
+    if (dtype != MAXSIM_FP16 && dtype != MAXSIM_BF16 && dtype != MAXSIM_INT8) return MAXSIM_ERR_UNSUPPORTED;
+    if (!layout || sm_count <= 0 || n_q < 0 || lq_max < 0 || n_docs < 0 || total_d_tokens < 0)
+        return MAXSIM_ERR_INVALID_ARGUMENT;
+    for (int k = 0; k < 5; ++k) layout[k] = 0;
+    if (n_q == 0 || n_docs == 0 || lq_max == 0 || total_d_tokens == 0) return MAXSIM_OK;   // no forward kernel
+    const bool int8 = dtype == MAXSIM_INT8;
+    const int64_t rows = static_cast<int64_t>(n_q) * lq_padded(lq_max);
+    if (rows > INT32_MAX / 2) return MAXSIM_ERR_INVALID_ARGUMENT;
+    const LaunchLayout l =
+        launch_layout(rows, forward_mtiles(rows, int8), int8, sm_count, with_argmax != 0, total_d_tokens, n_docs);
+    if (l.groups * l.parts > INT32_MAX) return MAXSIM_ERR_INVALID_ARGUMENT;
+    layout[0] = l.nmt;
+    layout[1] = l.ctas_per_sm;
+    layout[2] = static_cast<int32_t>(l.groups);
+    layout[3] = static_cast<int32_t>(l.parts);
+    layout[4] = l.ksplit ? 1 : 0;
+    return MAXSIM_OK;
 }
 
 maxsim_status_t maxsim_selftest_bounded_wait(uint32_t limit_us, void *stream_) {
