@@ -25,7 +25,7 @@ from ._build import build_oracle, library_path
 __all__ = [
     "decode", "forward_bits", "forward_f64", "forward_i8", "forward_i8_token", "dot_bits",
     "backward_f64", "build_csr", "topk", "rerank_two_stage", "chamfer_nn", "chamfer_forward",
-    "chamfer_backward", "chamfer_csr", "DTYPE_CODES",
+    "chamfer_backward", "chamfer_csr", "chamfer_pair_dist", "dot_i8_token", "DTYPE_CODES",
 ]
 
 DTYPE_CODES = {"fp16": 0, "bf16": 1}
@@ -65,11 +65,16 @@ def _load():
                                       I64, _vp, _vp, _vp, _vp, _vp]
     lib.oracle_forward_i8.restype = INT
     lib.oracle_forward_i8_token.argtypes = [_i8p, _f32p, _i32p, I32, I32, _i8p, _f32p, _i32p, I32, I32,
-                                            I64, _vp, _vp, _vp, _vp, _vp]
+                                            I64, _vp, _vp, _vp, _vp, _vp, _vp]
     lib.oracle_forward_i8_token.restype = INT
-    lib.oracle_chamfer_nn.argtypes = [_f32p, _i32p, _f32p, _i32p, I32, _f32p, _i32p]
+    lib.oracle_dot_i8_token.argtypes = [_i8p, I32, _i8p, _f32p, _i32p, I32, I64, _i32p, _i32p, _i32p, _i32p,
+                                        _f64p]
+    lib.oracle_dot_i8_token.restype = INT
+    lib.oracle_chamfer_pair_dist.argtypes = [_f32p, _f32p, I64, _i32p, _i32p, _f64p]
+    lib.oracle_chamfer_pair_dist.restype = INT
+    lib.oracle_chamfer_nn.argtypes = [_f32p, _i32p, _f32p, _i32p, I32, _f64p, _i32p, _vp]
     lib.oracle_chamfer_nn.restype = INT
-    lib.oracle_chamfer_reduce.argtypes = [_f32p, _i32p, _f32p, _i32p, I32, _f64p]
+    lib.oracle_chamfer_reduce.argtypes = [_f64p, _i32p, _f64p, _i32p, I32, _f64p]
     lib.oracle_chamfer_reduce.restype = INT
     lib.oracle_chamfer_backward.argtypes = [_f32p, _i32p, _f32p, _i32p, I32, _i32p, _i32p, _f64p, _f64p, _f64p]
     lib.oracle_chamfer_backward.restype = INT
@@ -247,11 +252,13 @@ def forward_i8(Q, q_lens, D, cu_seqlens, q_scale, d_scale, pairs=None, threads=1
 def forward_i8_token(Q, q_scales, q_lens, D, d_scales, cu_seqlens, pairs=None, want_rowmax=False,
                      threads=1):
     """Flash-MaxSim §4.3.1 INT8 x INT8 MaxSim with one scale per token (the
-    reading in oracle.c, R6): the value ranked is fp32(dot * d_scale[t]),
-    the row maximum is multiplied by the query token's scale and summed in
-    binary64.  Q int8 [n_q, lq_max, dim], q_scales f32 [n_q, lq_max], D int8
-    [total, dim], d_scales f32 [total].  Returns dict(score [P] f64, argmax
-    [P, lq_max] i32, and rowmax [P, lq_max] f32 when want_rowmax)."""
+    reading in oracle.c, R6): the value ranked is the exact product
+    dot * d_scale[t] in binary64, the row maximum (lowest t on ties) is
+    multiplied by the query token's scale and summed in binary64.  Q int8
+    [n_q, lq_max, dim], q_scales f32 [n_q, lq_max], D int8 [total, dim],
+    d_scales f32 [total].  Returns dict(score [P] f64, argmax [P, lq_max]
+    i32, and when want_rowmax, rowmax [P, lq_max] f64 and gap [P, lq_max] f64
+    = top-1 minus top-2)."""
     lib = _load()
     Q = _c(Q, np.int8)
     D = _c(D, np.int8)
@@ -265,7 +272,8 @@ def forward_i8_token(Q, q_scales, q_lens, D, d_scales, cu_seqlens, pairs=None, w
     P = pq.shape[0]
     score = np.empty(P, np.float64)
     argmax = np.empty((P, lq_max), np.int32)
-    rowmax = np.empty((P, lq_max), np.float32) if want_rowmax else None
+    rowmax = np.empty((P, lq_max), np.float64) if want_rowmax else None
+    gap = np.empty((P, lq_max), np.float64) if want_rowmax else None
     Dflat = D.reshape(-1) if D.size else np.zeros(1, np.int8)
     dsflat = ds.reshape(-1) if ds.size else np.zeros(1, np.float32)
 
@@ -275,7 +283,8 @@ def forward_i8_token(Q, q_scales, q_lens, D, d_scales, cu_seqlens, pairs=None, w
         rc = lib.oracle_forward_i8_token(Q.reshape(-1), qs.reshape(-1), q_lens, n_q, lq_max, Dflat, dsflat,
                                          cu, n_docs, dim, e - s, _ptr(pq[s:e]), _ptr(pb[s:e]),
                                          _ptr(score[s:e]), _ptr(argmax[s:e]),
-                                         _ptr(None if rowmax is None else rowmax[s:e]))
+                                         _ptr(None if rowmax is None else rowmax[s:e]),
+                                         _ptr(None if gap is None else gap[s:e]))
         if rc != 0:
             raise ValueError(f"oracle_forward_i8_token failed ({rc})")
 
@@ -283,6 +292,23 @@ def forward_i8_token(Q, q_scales, q_lens, D, d_scales, cu_seqlens, pairs=None, w
     out = {"score": score, "argmax": argmax}
     if want_rowmax:
         out["rowmax"] = rowmax
+        out["gap"] = gap
+    return out
+
+
+def dot_i8_token(Q, D, d_scales, cu_seqlens, q, b, i, t):
+    """Exact ranked value dot(Q[q,i], D[cu[b]+t]) * d_scales[cu[b]+t] (R6)
+    for arrays of (q, b, i, t)."""
+    lib = _load()
+    Q = _c(Q, np.int8)
+    D = _c(D, np.int8)
+    ds = _c(d_scales, np.float32)
+    cu = _c(cu_seqlens, np.int32)
+    n_q, lq_max, dim = Q.shape
+    q, b, i, t = (_c(x, np.int32).reshape(-1) for x in (q, b, i, t))
+    out = np.empty(q.shape[0], np.float64)
+    lib.oracle_dot_i8_token(Q.reshape(-1), lq_max, D.reshape(-1), ds.reshape(-1), cu, dim, q.shape[0],
+                            q, b, i, t, out)
     return out
 
 
@@ -341,32 +367,50 @@ def _pts(a):
     return a if a.size else np.zeros((1, 3), np.float32)
 
 
-def chamfer_nn(S, cu_s, T, cu_t):
-    """Nearest target of every source point (reading R7 in oracle.c): binary32
-    squared distances [total_s] and target indices local to the item [total_s]."""
+def chamfer_nn(S, cu_s, T, cu_t, want_gap=False):
+    """Nearest target of every source point (reading R7 in oracle.c): binary64
+    squared distances [total_s] and target indices local to the item
+    [total_s]; with want_gap also the second-smallest distance minus the
+    smallest [total_s]."""
     lib = _load()
     cu_s, cu_t = _c(cu_s, np.int32), _c(cu_t, np.int32)
     n = int(cu_s[-1])
-    dist = np.empty(max(n, 1), np.float32)
+    dist = np.empty(max(n, 1), np.float64)
     arg = np.empty(max(n, 1), np.int32)
-    rc = lib.oracle_chamfer_nn(_pts(S).reshape(-1), cu_s, _pts(T).reshape(-1), cu_t, cu_s.shape[0] - 1, dist, arg)
+    gap = np.empty(max(n, 1), np.float64) if want_gap else None
+    rc = lib.oracle_chamfer_nn(_pts(S).reshape(-1), cu_s, _pts(T).reshape(-1), cu_t, cu_s.shape[0] - 1, dist, arg,
+                               _ptr(gap))
     if rc != 0:
         raise ValueError("oracle_chamfer_nn failed")
+    if want_gap:
+        return dist[:n], arg[:n], gap[:n]
     return dist[:n], arg[:n]
+
+
+def chamfer_pair_dist(S, T, s_idx, t_idx):
+    """Squared distances (R7) of (source, target) index pairs (global indices
+    into the packed point arrays), binary64."""
+    lib = _load()
+    s_idx, t_idx = _c(s_idx, np.int32).reshape(-1), _c(t_idx, np.int32).reshape(-1)
+    out = np.empty(s_idx.shape[0], np.float64)
+    lib.oracle_chamfer_pair_dist(_pts(S).reshape(-1), _pts(T).reshape(-1), s_idx.shape[0], s_idx, t_idx, out)
+    return out
 
 
 def chamfer_forward(P, cu_p, Q, cu_q):
     """Chamfer distance of every item (Flash-MaxSim §4.2, "Generalization to
-    Chamfer Distance"): dict(cd [B] f64, dist_pq, arg_pq, dist_qp, arg_qp)."""
+    Chamfer Distance"), binary64: dict(cd [B], dist_pq, arg_pq, gap_pq,
+    dist_qp, arg_qp, gap_qp)."""
     lib = _load()
     cu_p, cu_q = _c(cu_p, np.int32), _c(cu_q, np.int32)
-    d_pq, a_pq = chamfer_nn(P, cu_p, Q, cu_q)
-    d_qp, a_qp = chamfer_nn(Q, cu_q, P, cu_p)
+    d_pq, a_pq, g_pq = chamfer_nn(P, cu_p, Q, cu_q, want_gap=True)
+    d_qp, a_qp, g_qp = chamfer_nn(Q, cu_q, P, cu_p, want_gap=True)
     B = cu_p.shape[0] - 1
     cd = np.empty(max(B, 1), np.float64)
-    lib.oracle_chamfer_reduce(np.ascontiguousarray(d_pq) if d_pq.size else np.zeros(1, np.float32), cu_p,
-                              np.ascontiguousarray(d_qp) if d_qp.size else np.zeros(1, np.float32), cu_q, B, cd)
-    return {"cd": cd[:B], "dist_pq": d_pq, "arg_pq": a_pq, "dist_qp": d_qp, "arg_qp": a_qp}
+    lib.oracle_chamfer_reduce(np.ascontiguousarray(d_pq) if d_pq.size else np.zeros(1, np.float64), cu_p,
+                              np.ascontiguousarray(d_qp) if d_qp.size else np.zeros(1, np.float64), cu_q, B, cd)
+    return {"cd": cd[:B], "dist_pq": d_pq, "arg_pq": a_pq, "gap_pq": g_pq, "dist_qp": d_qp, "arg_qp": a_qp,
+            "gap_qp": g_qp}
 
 
 def chamfer_backward(P, cu_p, Q, cu_q, arg_pq, arg_qp, grad):

@@ -27,21 +27,19 @@
  *       end, where raw is the exact int64 sum of int32 row maxima.
  *   R6  INT8 with one scale per token (the per-token quantisation of
  *       Flash-MaxSim §4.3.1): the value ranked for query token i and document
- *       token t is the single-precision product fp32(dot * s_D[t]) of the
- *       exact integer dot product (below 2^24, so exact in binary32) and the
- *       document token's scale; the row maximum and its lowest index are
- *       taken on those values (the decision is made in binary32, the
- *       precision the kernel ranks in), the query token's scale multiplies
- *       the maximum, and the sum over query tokens runs in binary64.
+ *       token t is the real product dot * s_D[t] of the exact integer dot
+ *       product and the document token's scale, evaluated in binary64 (an
+ *       integer below 2^24 times a binary32 scale is exact there); the row
+ *       maximum and its lowest index are taken on those exact values, the
+ *       query token's scale multiplies the maximum, and the sum over query
+ *       tokens runs in binary64.
  *   R7  Chamfer distance (Flash-MaxSim §4.2 "Generalization to Chamfer
- *       Distance"): the squared distance ranked for a source point s and a
- *       target point t is the binary32 value
- *           fma(dz, dz, fma(dy, dy, dx * dx)),  dx = s.x - t.x  (each step
- *       rounded to nearest even), the precision and order the kernel ranks
- *       in; the nearest target is the lowest index attaining the minimum; an
- *       empty target set gives +inf and index -1.  The means over points and
- *       the gradients are evaluated in binary64.  A mean over an empty set is
- *       0.
+ *       Distance"): the squared Euclidean distance of a source point s and a
+ *       target point t, evaluated in binary64 from the binary32 coordinates
+ *       as (s.x - t.x)^2 + (s.y - t.y)^2 + (s.z - t.z)^2; the nearest target
+ *       is the lowest index attaining the minimum; an empty target set gives
+ *       +inf and index -1.  The means over points and the gradients are
+ *       evaluated in binary64.  A mean over an empty set is 0.
  *
  * Parity status: every function here is pinned by CPU tests against closed
  * forms, invariants, brute force and finite differences (tests/test_oracle_*).
@@ -324,14 +322,16 @@ int oracle_forward_i8(const int8_t *Q, const int32_t *q_lens, int32_t n_q, int32
 /*
  * INT8 with one symmetric scale per token (R6).  q_scales [n_q, lq_max],
  * d_scales [total]; outputs per pair: score (binary64; -inf for an empty
- * document and a query with tokens), argmax [.., lq_max] and, when rowmax is
- * non-NULL, the binary32 row maxima [.., lq_max] (-inf for padding / empty).
+ * document and a query with tokens), argmax [.., lq_max]; when rowmax / gap
+ * are non-NULL, the binary64 row maxima and the gap from the maximum to the
+ * largest value over the other tokens [.., lq_max] (-inf / +inf for padding
+ * and empty documents, +inf for a document of one token).
  */
 int oracle_forward_i8_token(const int8_t *Q, const float *q_scales, const int32_t *q_lens, int32_t n_q,
                             int32_t lq_max, const int8_t *D, const float *d_scales,
                             const int32_t *cu_seqlens, int32_t n_docs, int32_t dim,
                             int64_t n_pairs, const int32_t *pair_q, const int32_t *pair_b,
-                            double *score, int32_t *argmax, float *rowmax)
+                            double *score, int32_t *argmax, double *rowmax, double *gap)
 {
     if (n_q < 0 || n_docs < 0 || lq_max < 0 || dim <= 0) return -1;
     if (pair_q == NULL) n_pairs = (int64_t)n_q * n_docs;
@@ -346,32 +346,57 @@ int oracle_forward_i8_token(const int8_t *Q, const float *q_scales, const int32_
         double sum = 0.0;
         int empty = 0;
         for (int32_t i = 0; i < lq_max; ++i) {
+            int64_t o = p * lq_max + i;
             if (i >= lq) {
-                if (argmax) argmax[p * lq_max + i] = -1;
-                if (rowmax) rowmax[p * lq_max + i] = -INFINITY;
+                if (argmax) argmax[o] = -1;
+                if (rowmax) rowmax[o] = -INFINITY;
+                if (gap) gap[o] = INFINITY;
                 continue;
             }
             const int8_t *qi = Q + ((int64_t)q * lq_max + i) * dim;
-            float best = -INFINITY;
+            double best = -INFINITY, second = -INFINITY;
             int64_t arg = -1;
             for (int64_t t = 0; t < ld; ++t) {
                 const int8_t *dt = D + (t0 + t) * dim;
                 int64_t v = 0;
                 for (int k = 0; k < dim; ++k) v += (int64_t)qi[k] * (int64_t)dt[k];
-                if (v > 16777216 || v < -16777216) return -3;  /* exact in binary32 */
-                float dot = (float)v;
-                float scaled = dot * d_scales[t0 + t];          /* one binary32 rounding */
+                if (v > 16777216 || v < -16777216) return -3;  /* < 2^24: the product below is exact */
+                double scaled = (double)v * (double)d_scales[t0 + t];
                 if (arg < 0 || scaled > best) {                  /* lowest t on ties */
+                    second = best;
                     best = scaled;
                     arg = t;
+                } else if (scaled > second) {
+                    second = scaled;
                 }
             }
             if (arg < 0) empty = 1;
-            else sum += (double)q_scales[(int64_t)q * lq_max + i] * (double)best;
-            if (argmax) argmax[p * lq_max + i] = (int32_t)arg;
-            if (rowmax) rowmax[p * lq_max + i] = best;
+            else sum += (double)q_scales[(int64_t)q * lq_max + i] * best;
+            if (argmax) argmax[o] = (int32_t)arg;
+            if (rowmax) rowmax[o] = best;
+            if (gap) gap[o] = ld >= 2 ? best - second : INFINITY;
         }
         score[p] = empty ? -INFINITY : sum;
+    }
+    return 0;
+}
+
+/*
+ * Exact ranked values dot(Q_{q,i}, D_{cu[b]+t}) * s_D[cu[b]+t] (R6) for n
+ * given (q, b, i, t) tuples -- used to judge an argmax reported by the
+ * kernel against the true maximum.
+ */
+int oracle_dot_i8_token(const int8_t *Q, int32_t lq_max, const int8_t *D, const float *d_scales,
+                        const int32_t *cu_seqlens, int32_t dim, int64_t n, const int32_t *q,
+                        const int32_t *b, const int32_t *i, const int32_t *t, double *out)
+{
+    for (int64_t k = 0; k < n; ++k) {
+        const int8_t *qi = Q + ((int64_t)q[k] * lq_max + i[k]) * dim;
+        int64_t row = (int64_t)cu_seqlens[b[k]] + t[k];
+        const int8_t *dt = D + row * dim;
+        int64_t v = 0;
+        for (int c = 0; c < dim; ++c) v += (int64_t)qi[c] * (int64_t)dt[c];
+        out[k] = (double)v * (double)d_scales[row];
     }
     return 0;
 }
@@ -382,50 +407,64 @@ int oracle_forward_i8_token(const int8_t *Q, const float *q_scales, const int32_
 /* row of three binary32 coordinates.                                        */
 /* ------------------------------------------------------------------------- */
 
-static float chamfer_d2(const float *s, const float *t)
+static double chamfer_d2(const float *s, const float *t)
 {
-    float dx = s[0] - t[0];
-    float dy = s[1] - t[1];
-    float dz = s[2] - t[2];
-    float xx = dx * dx;
-    return fmaf(dz, dz, fmaf(dy, dy, xx));
+    double dx = (double)s[0] - (double)t[0];
+    double dy = (double)s[1] - (double)t[1];
+    double dz = (double)s[2] - (double)t[2];
+    return dx * dx + dy * dy + dz * dz;
 }
 
-/* Nearest target of every source point: dist [total_s] (binary32), arg
- * [total_s] (index local to the item's target set, -1 when it is empty). */
+/* Nearest target of every source point: dist [total_s] (binary64), arg
+ * [total_s] (index local to the item's target set, -1 when it is empty) and,
+ * when gap is non-NULL, the second-smallest distance minus the smallest
+ * (+inf with fewer than two targets). */
 int oracle_chamfer_nn(const float *S, const int32_t *cu_s, const float *T, const int32_t *cu_t,
-                      int32_t n_items, float *dist, int32_t *arg)
+                      int32_t n_items, double *dist, int32_t *arg, double *gap)
 {
     if (n_items < 0) return -1;
     for (int32_t b = 0; b < n_items; ++b) {
         int64_t t0 = cu_t[b], m = (int64_t)cu_t[b + 1] - t0;
         for (int64_t s = cu_s[b]; s < cu_s[b + 1]; ++s) {
-            float best = INFINITY;
+            double best = INFINITY, second = INFINITY;
             int64_t a = -1;
             for (int64_t t = 0; t < m; ++t) {
-                float d = chamfer_d2(S + 3 * s, T + 3 * (t0 + t));
+                double d = chamfer_d2(S + 3 * s, T + 3 * (t0 + t));
                 if (a < 0 || d < best) {     /* strict after the first: lowest t on ties */
+                    second = best;
                     best = d;
                     a = t;
+                } else if (d < second) {
+                    second = d;
                 }
             }
             dist[s] = best;
             arg[s] = (int32_t)a;
+            if (gap) gap[s] = m >= 2 ? second - best : INFINITY;
         }
     }
     return 0;
 }
 
+/* Squared distances (R7) of n given (source, target) index pairs of the
+ * packed point arrays. */
+int oracle_chamfer_pair_dist(const float *S, const float *T, int64_t n, const int32_t *si, const int32_t *ti,
+                             double *out)
+{
+    for (int64_t k = 0; k < n; ++k) out[k] = chamfer_d2(S + 3 * (int64_t)si[k], T + 3 * (int64_t)ti[k]);
+    return 0;
+}
+
 /* cd[b] = mean over P of its nearest-target distance + mean over Q of its
- * nearest-source distance, from the binary32 distances, in binary64. */
-int oracle_chamfer_reduce(const float *dist_pq, const int32_t *cu_p, const float *dist_qp, const int32_t *cu_q,
+ * nearest-source distance, in binary64. */
+int oracle_chamfer_reduce(const double *dist_pq, const int32_t *cu_p, const double *dist_qp, const int32_t *cu_q,
                           int32_t n_items, double *cd)
 {
     for (int32_t b = 0; b < n_items; ++b) {
         double a = 0.0, c = 0.0;
         int64_t n = (int64_t)cu_p[b + 1] - cu_p[b], m = (int64_t)cu_q[b + 1] - cu_q[b];
-        for (int64_t i = cu_p[b]; i < cu_p[b + 1]; ++i) a += (double)dist_pq[i];
-        for (int64_t j = cu_q[b]; j < cu_q[b + 1]; ++j) c += (double)dist_qp[j];
+        for (int64_t i = cu_p[b]; i < cu_p[b + 1]; ++i) a += dist_pq[i];
+        for (int64_t j = cu_q[b]; j < cu_q[b + 1]; ++j) c += dist_qp[j];
         cd[b] = (n ? a / (double)n : 0.0) + (m ? c / (double)m : 0.0);
     }
     return 0;
