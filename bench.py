@@ -549,6 +549,103 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------------ single cases
+
+# ``--case NAME``: one library entry point on seeded synthetic inputs, called
+# ``--reps`` times on cuda:0 (no timing, no JSON line) -- the command the
+# committed ncu summaries under profiles/ profile.
+
+def _case_forward(m, syn, torch, a):
+    w = syn.WORKLOADS[a.workload]
+    x = syn.make_inputs(w, device="cuda", n_docs=a.n_docs)
+    kw = dict(q_scale=x["q_scale"], d_scale=x["d_scale"])
+    s, am, _ = m.maxsim_forward(x["Q"], x["q_lens"], x["D"], x["cu_seqlens"], with_argmax=not a.value_only, **kw)
+    for _ in range(a.reps - 1):
+        m.maxsim_forward(x["Q"], x["q_lens"], x["D"], x["cu_seqlens"], with_argmax=not a.value_only, scores=s,
+                         argmax=am, **kw)
+
+
+def _case_int8_token(m, syn, torch, a):
+    w = syn.WORKLOADS["int8_varlen"]
+    n_docs = a.n_docs or w.n_docs
+    cu = syn.cu_seqlens_from_lengths(syn.doc_lengths(w.n_docs, w.ld_lo, w.ld_hi, w.seed)[:n_docs]).cuda()
+    Q8, qs = syn.unit_tokens_int8_per_token(w.n_q * w.lq, w.dim, w.seed + 1, "cuda")
+    D8, ds = syn.unit_tokens_int8_per_token(int(cu[-1]), w.dim, w.seed + 2, "cuda")
+    ql = torch.full((w.n_q,), w.lq, dtype=torch.int32, device="cuda")
+    for _ in range(a.reps):
+        m.maxsim_forward_int8_per_token(Q8.view(w.n_q, w.lq, w.dim), qs.view(w.n_q, w.lq), ql, D8, ds, cu,
+                                        with_argmax=not a.value_only)
+
+
+def _case_backward(m, syn, torch, a):
+    w = syn.WORKLOADS[a.workload]
+    x = syn.make_inputs(w, device="cuda", n_docs=a.n_docs)
+    Q, ql, D, cu = x["Q"], x["q_lens"], x["D"], x["cu_seqlens"]
+    s, am, _ = m.maxsim_forward(Q, ql, D, cu)
+    g = torch.softmax(s / 0.05, dim=1).contiguous()
+    for _ in range(a.reps):
+        m.maxsim_backward(g, am, Q, ql, D, cu)
+
+
+def _case_chamfer(m, syn, torch, a):
+    g = torch.Generator("cuda").manual_seed(0)
+    P = torch.rand((a.points, 3), generator=g, device="cuda")
+    Q = torch.rand((a.points, 3), generator=g, device="cuda")
+    cu = torch.tensor([0, a.points], dtype=torch.int32, device="cuda")
+    for _ in range(a.reps):
+        _, _, apq, _, aqp = m.maxsim_chamfer_forward(P, cu, Q, cu)
+        m.maxsim_chamfer_backward(torch.ones(1, device="cuda"), P, cu, Q, cu, apq, aqp)
+
+
+def _case_rerank(m, syn, torch, a):
+    """Two-stage scan on the INT8 varlen workload: 1,000 candidates, 100 kept."""
+    w = syn.WORKLOADS["int8_varlen"]
+    n_docs = a.n_docs or w.n_docs
+    cu = syn.cu_seqlens_from_lengths(syn.doc_lengths(w.n_docs, w.ld_lo, w.ld_hi, w.seed)[:n_docs]).cuda()
+    total = int(cu[-1])
+    Q8, qs = syn.unit_tokens_int8(w.n_q * w.lq, w.dim, w.seed + 1, "cuda")
+    D8, ds = syn.unit_tokens_int8(total, w.dim, w.seed + 2, "cuda")
+    Q16 = syn.unit_tokens(w.n_q * w.lq, w.dim, w.seed + 1, "fp16", "cuda").view(w.n_q, w.lq, w.dim)
+    D16 = syn.unit_tokens(total, w.dim, w.seed + 2, "fp16", "cuda")
+    ql = torch.full((w.n_q,), w.lq, dtype=torch.int32, device="cuda")
+    for _ in range(a.reps):
+        m.maxsim_rerank_two_stage(Q8.view(w.n_q, w.lq, w.dim), D8, Q16, D16, ql, cu, k_candidates=1000, k=100,
+                                  q_scale=qs, d_scale=ds, max_doc_len=w.ld_hi)
+
+
+def _case_host(m, syn, torch, a):
+    """Out-of-core forward: the ColBERT workload's corpus in pinned host
+    memory, streamed in blocks of 5,000 documents."""
+    w = syn.WORKLOADS["colbert_varlen"]
+    x = syn.make_inputs(w, device="cuda", n_docs=a.n_docs)
+    D_h = x["D"].cpu().pin_memory()
+    cu_h = x["cu_seqlens"].cpu().pin_memory()
+    for _ in range(a.reps):
+        m.maxsim_forward_host(x["Q"], x["q_lens"], D_h, cu_h, block_docs=5000, block_tokens=5000 * w.ld_hi,
+                              with_argmax=True)
+    torch.cuda.synchronize()
+
+
+CASES = {"forward": _case_forward, "int8-token": _case_int8_token, "backward": _case_backward,
+         "chamfer": _case_chamfer, "rerank": _case_rerank, "host": _case_host}
+
+
+def run_case(args) -> int:
+    import torch
+
+    import late_interaction_retrieval_maxsim_gb300 as m
+    from late_interaction_retrieval_maxsim_gb300 import synthetic as syn
+    torch.cuda.set_device(0)
+    m.load_library()
+    CASES[args.case](m, syn, torch, args)
+    torch.cuda.synchronize()
+    status = m.maxsim_device_status()
+    if status != 0:
+        print(f"device status word {status:#x}", file=sys.stderr)
+        return 1
+    return 0
+
+
 # ---------------------------------------------------------------- reference
 
 def run_reference(args):
@@ -611,7 +708,16 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
     ap.add_argument("--ref-docs", type=int, default=32, help="documents per reference step")
+    ap.add_argument("--case", choices=sorted(CASES), default=None,
+                    help="run one entry point on synthetic inputs (for profilers) instead of the benchmark")
+    ap.add_argument("--workload", default="colbert_varlen", help="--case: workload name (synthetic.WORKLOADS)")
+    ap.add_argument("--n-docs", type=int, default=None, help="--case: first n documents of the workload")
+    ap.add_argument("--points", type=int, default=20_000, help="--case chamfer: points per cloud")
+    ap.add_argument("--reps", type=int, default=2, help="--case: calls of the entry point")
+    ap.add_argument("--value-only", action="store_true", help="--case: forward without the argmax output")
     args = ap.parse_args()
+    if args.case is not None:
+        sys.exit(run_case(args))
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":

@@ -131,8 +131,10 @@ maxsim_status_t maxsim_forward(const void *Q, const int32_t *q_lens, int32_t n_q
  *     one million FP32 partial sums: e.g. a 1024-token query against
  *     32,000 documents).
  *   - The first call on a device looks up the array's device address (with
- *     that device current) and caches it; make that first call before any
- *     stream capture.
+ *     that device current) and caches it with the device's context; make
+ *     that first call before any stream capture.  A call that finds another
+ *     context current on the device (after cudaDeviceReset, say) looks the
+ *     address up again.
  *   - Every call shares the one array and leaves its contents behind; calls
  *     whose work overlaps on the GPU (other streams, other threads) race on
  *     it and must be serialised by the caller.

@@ -178,6 +178,40 @@ def _require(t, name, dtype=None, device=None, contiguous=True):
         raise ValueError(f"{name} is on {t.device}, expected {device}")
 
 
+def _check_qd(Q, D):
+    """Shapes of a forward's Q [n_q, lq_max, dim] and D [total, dim]."""
+    torch = _torch()
+    if not isinstance(Q, torch.Tensor) or not isinstance(D, torch.Tensor):
+        raise TypeError("Q and D must be tensors")
+    if Q.dim() != 3 or D.dim() != 2 or Q.shape[2] != D.shape[1]:
+        raise ValueError("Q must be [n_q, lq_max, dim] and D [total, dim]")
+
+
+def _check_output(t, name, shape, dtype, device):
+    """A caller-provided output: exactly the shape, dtype and device the
+    kernels write (they index it without bounds), contiguous."""
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _check_forward_outputs(n_q, n_docs, lq_max, device, scores, argmax, raw_scores):
+    torch = _torch()
+    _check_output(scores, "scores", (n_q, n_docs), torch.float32, device)
+    if argmax is not None:
+        _check_output(argmax, "argmax", (n_q, n_docs, lq_max), torch.int32, device)
+    if raw_scores is not None:
+        _check_output(raw_scores, "raw_scores", (n_q, n_docs), torch.int64, device)
+
+
 def maxsim_abi_version() -> int:
     return int(load_library().maxsim_abi_version())
 
@@ -202,16 +236,22 @@ def maxsim_forward(Q, q_lens, D, cu_seqlens, *, with_argmax: bool = True, q_scal
     lq_max] int32 or None, raw_scores [n_q, n_docs] int64 or None)."""
     torch = _torch()
     lib = load_library()
+    _check_qd(Q, D)
+    n_q, lq_max, dim = Q.shape
+    n_docs = cu_seqlens.numel() - 1
+    total = D.shape[0]
+    # caller-provided outputs are written without bounds checks
+    if scores is not None:
+        _check_output(scores, "scores", (n_q, n_docs), torch.float32, Q.device)
+    if argmax is not None and with_argmax:
+        _check_output(argmax, "argmax", (n_q, n_docs, lq_max), torch.int32, Q.device)
     _require(Q, "Q")
     dev = Q.device
     _require(D, "D", dtype=Q.dtype, device=dev)
     _require(q_lens, "q_lens", torch.int32, dev)
     _require(cu_seqlens, "cu_seqlens", torch.int32, dev)
-    if Q.dim() != 3 or D.dim() != 2 or Q.shape[2] != D.shape[1]:
-        raise ValueError("Q must be [n_q, lq_max, dim] and D [total, dim]")
-    n_q, lq_max, dim = Q.shape
-    n_docs = cu_seqlens.numel() - 1
-    total = D.shape[0]
+    if q_lens.shape != (n_q,):
+        raise ValueError(f"q_lens must have shape ({n_q},)")
     code = _dtype_code(Q)
     if scores is None:
         scores = torch.empty((n_q, n_docs), dtype=torch.float32, device=dev)
@@ -221,6 +261,9 @@ def maxsim_forward(Q, q_lens, D, cu_seqlens, *, with_argmax: bool = True, q_scal
         argmax = None
     if code == 2 and want_raw and raw_scores is None:
         raw_scores = torch.empty((n_q, n_docs), dtype=torch.int64, device=dev)
+    if code != 2:
+        raw_scores = None
+    _check_forward_outputs(n_q, n_docs, lq_max, dev, scores, argmax, raw_scores)
     ws_bytes = maxsim_forward_workspace_size(n_q, lq_max, n_docs, code, dim)
     if ws_bytes and (workspace is None or workspace.numel() < ws_bytes):
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
@@ -242,16 +285,24 @@ def maxsim_forward_noalloc(Q, q_lens, D, cu_seqlens, scores, *, argmax=None, raw
     overlap on the GPU share that array and must be serialised."""
     torch = _torch()
     lib = load_library()
+    _check_qd(Q, D)
+    n_q, lq_max, dim = Q.shape
+    n_docs = cu_seqlens.numel() - 1
+    # the outputs are written without bounds checks: their shapes, dtypes and
+    # device are checked first, before anything reaches the library
+    _check_forward_outputs(n_q, n_docs, lq_max, Q.device, scores, argmax, raw_scores)
+    if raw_scores is not None and Q.dtype != torch.int8:
+        raise ValueError("raw_scores is an INT8 output")
     _require(Q, "Q")
     dev = Q.device
     _require(D, "D", dtype=Q.dtype, device=dev)
     _require(q_lens, "q_lens", torch.int32, dev)
     _require(cu_seqlens, "cu_seqlens", torch.int32, dev)
-    _require(scores, "scores", torch.float32, dev)
-    n_q, lq_max, dim = Q.shape
+    if q_lens.shape != (n_q,):
+        raise ValueError(f"q_lens must have shape ({n_q},)")
     with torch.cuda.device(dev):
         st = lib.maxsim_forward_noalloc(_ptr(Q), _ptr(q_lens), n_q, lq_max, _ptr(D), _ptr(cu_seqlens),
-                                        cu_seqlens.numel() - 1, D.shape[0], dim, _dtype_code(Q),
+                                        n_docs, D.shape[0], dim, _dtype_code(Q),
                                         float(q_scale), float(d_scale), _ptr(scores), _ptr(raw_scores),
                                         _ptr(argmax), _stream(stream))
     _check("maxsim_forward_noalloc", st)

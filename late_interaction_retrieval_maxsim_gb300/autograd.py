@@ -14,8 +14,8 @@ against 0.98 ms forward, 6 us saved), so the plain ``maxsim_forward`` /
 kernels; this module only routes tensors.
 
 Gradients are computed in FP32 by the kernels and returned in the inputs'
-dtype (autograd requires it); pass ``fp32_grads=True`` to keep the FP32
-buffers in ``MaxSimGrads`` as well.
+dtype (autograd requires a gradient of its input's dtype); callers that need
+the FP32 gradients call ``maxsim_backward`` directly.
 """
 from __future__ import annotations
 

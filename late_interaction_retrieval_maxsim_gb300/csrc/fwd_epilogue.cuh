@@ -57,10 +57,13 @@ __device__ __forceinline__ float chunk_max(const uint32_t (&r)[32], int lo, int 
     return fmax3(fmax3(z0, z1, z2), y[9], y[10]);
 }
 
-// True when the one-instruction indicator below is exact for maximum cm.
+// True when the one-instruction indicator below is exact for maximum cm:
+// every finite value below cm then lies at least 2^-100 below it.  The
+// closest float below cm is half an ulp of cm away when cm is a power of
+// two (2^-101 for cm = 2^-77), so the bound is 2^-76, not 2^-77.
 __device__ __forceinline__ bool fast_indicator_ok(float cm) {
     const float x = fabsf(cm);
-    return x >= 0x1p-77f && x < 0x1p27f;
+    return x >= 0x1p-76f && x < 0x1p27f;
 }
 
 // The 32-bit mask from its two 16-bit halves, each held as the float
@@ -77,8 +80,9 @@ __device__ __forceinline__ uint32_t mask_from_halves(float lo, float hi) {
 // (the ALU pipe that compares and selects use issues at half rate): with
 // S = 2^100 and C = cm * S (exact), fma.sat(value, -S, C) = sat(S * (cm -
 // value)) is 0 when value == cm and 1 when value < cm, because a nonzero
-// cm - value is at least one ulp of cm, >= 2^-100 when |cm| >= 2^-77, and C
-// stays finite when |cm| < 2^27 (`fast`).  Otherwise two saturating
+// cm - value is at least half an ulp of cm (the gap below a power of two),
+// >= 2^-100 when |cm| >= 2^-76, and C stays finite when |cm| < 2^27
+// (`fast`).  Otherwise two saturating
 // multiplies of (cm - value) by 2^127 and 2^23 reach 1 for every nonzero
 // finite difference.  Indicators are packed into the mask 8 at a time (sums
 // of distinct powers of two below 2^16 are exact in FP32).

@@ -216,20 +216,29 @@ struct EventSet {
     }
 };
 
+// The size limits of every forward: non-negative sizes, a token count the
+// kernels' 32-bit row indices cover, padded query rows within int32 and the
+// argmax element count within int64 bytes.
+maxsim_status_t check_forward_sizes(int32_t n_q, int32_t lq_max, int32_t n_docs, int64_t total_d_tokens) {
+    if (n_q < 0 || n_docs < 0 || lq_max < 0 || total_d_tokens < 0) return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (total_d_tokens > INT32_MAX - 256) return MAXSIM_ERR_INVALID_ARGUMENT;
+    const int64_t rows = static_cast<int64_t>(n_q) * (lq_max > 0 ? lq_padded(lq_max) : 1);
+    if (rows > INT32_MAX / 2 || static_cast<int64_t>(n_q) * n_docs * std::max(1, lq_max) > INT64_MAX / 8)
+        return MAXSIM_ERR_INVALID_ARGUMENT;
+    return MAXSIM_OK;
+}
+
 maxsim_status_t check_forward_args(const void *Q, const int32_t *q_lens, int32_t n_q, int32_t lq_max,
                                    int32_t n_docs, int64_t total_d_tokens, int32_t dim, maxsim_dtype_t dtype,
                                    float q_scale, float d_scale) {
     if (dtype != MAXSIM_FP16 && dtype != MAXSIM_BF16 && dtype != MAXSIM_INT8) return MAXSIM_ERR_UNSUPPORTED;
     if (dim != kDim) return MAXSIM_ERR_UNSUPPORTED;
-    if (n_q < 0 || n_docs < 0 || lq_max < 0 || total_d_tokens < 0) return MAXSIM_ERR_INVALID_ARGUMENT;
-    if (total_d_tokens > INT32_MAX - 256) return MAXSIM_ERR_INVALID_ARGUMENT;
+    const maxsim_status_t st = check_forward_sizes(n_q, lq_max, n_docs, total_d_tokens);
+    if (st != MAXSIM_OK) return st;
     if (n_q == 0 || n_docs == 0) return MAXSIM_OK;
     if (!q_lens) return MAXSIM_ERR_INVALID_ARGUMENT;
     if (lq_max > 0 && (!Q || !aligned16(Q))) return MAXSIM_ERR_INVALID_ARGUMENT;
     if (dtype == MAXSIM_INT8 && !(q_scale > 0.0f && d_scale > 0.0f)) return MAXSIM_ERR_INVALID_ARGUMENT;
-    const int64_t rows = static_cast<int64_t>(n_q) * (lq_max > 0 ? lq_padded(lq_max) : 1);
-    if (rows > INT32_MAX / 2 || static_cast<int64_t>(n_q) * n_docs * std::max(1, lq_max) > INT64_MAX / 8)
-        return MAXSIM_ERR_INVALID_ARGUMENT;
     return MAXSIM_OK;
 }
 
@@ -930,13 +939,13 @@ maxsim_status_t maxsim_forward_plan(int32_t n_q, int32_t lq_max, int32_t n_docs,
                                     maxsim_dtype_t dtype, int32_t with_argmax, int32_t sm_count,
                                     int32_t *layout) {
     if (dtype != MAXSIM_FP16 && dtype != MAXSIM_BF16 && dtype != MAXSIM_INT8) return MAXSIM_ERR_UNSUPPORTED;
-    if (!layout || sm_count <= 0 || n_q < 0 || lq_max < 0 || n_docs < 0 || total_d_tokens < 0)
-        return MAXSIM_ERR_INVALID_ARGUMENT;
+    if (!layout || sm_count <= 0) return MAXSIM_ERR_INVALID_ARGUMENT;
+    const maxsim_status_t st = check_forward_sizes(n_q, lq_max, n_docs, total_d_tokens);
+    if (st != MAXSIM_OK) return st;
     for (int k = 0; k < 5; ++k) layout[k] = 0;
     if (n_q == 0 || n_docs == 0 || lq_max == 0 || total_d_tokens == 0) return MAXSIM_OK;   // no forward kernel
     const bool int8 = dtype == MAXSIM_INT8;
     const int64_t rows = static_cast<int64_t>(n_q) * lq_padded(lq_max);
-    if (rows > INT32_MAX / 2) return MAXSIM_ERR_INVALID_ARGUMENT;
     const LaunchLayout l =
         launch_layout(rows, forward_mtiles(rows, int8), int8, sm_count, with_argmax != 0, total_d_tokens, n_docs);
     if (l.groups * l.parts > INT32_MAX) return MAXSIM_ERR_INVALID_ARGUMENT;

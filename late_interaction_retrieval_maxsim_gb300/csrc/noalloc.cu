@@ -12,10 +12,13 @@
 //
 // The array is a file-scope __device__ variable: each GPU that loads the
 // library holds kNoAllocScratchBytes for it until the process exits.  Its
-// device address is looked up once per device (the first call on a device,
-// with that device current) and cached.
+// device address is looked up once per device and context (the first call
+// with that device current, and again after the device's context has been
+// destroyed and re-created, e.g. by cudaDeviceReset) and cached.
 #include "maxsim.h"
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -30,8 +33,14 @@ constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
+struct ScratchAddress {
+    CUcontext ctx = nullptr;   // the context the address belongs to
+    void *ptr = nullptr;
+};
+
 std::mutex g_noalloc_mu;
-std::unordered_map<int, void *> g_noalloc_ptr;  // device ordinal -> device address of the array
+std::unordered_map<int, ScratchAddress> g_noalloc_ptr;   // device ordinal -> address in its current context
+PFN_cuCtxGetCurrent_v4000 g_ctx_get_current = nullptr;
 
 // Device address of the scratch array on the current device.  In host code
 // the array's name only stands in for the symbol; the real address must come
@@ -40,14 +49,28 @@ maxsim_status_t scratch_on_current_device(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MAXSIM_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_ctx_get_current == nullptr) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return MAXSIM_ERR_CUDA;
+        g_ctx_get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    }
+    // Before the runtime's first call on this device no context may be
+    // current (ctx == nullptr): the symbol lookup below makes the primary
+    // context current, and the context is read again after it.
+    CUcontext ctx = nullptr;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS) return MAXSIM_ERR_CUDA;
     auto it = g_noalloc_ptr.find(dev);
-    if (it == g_noalloc_ptr.end()) {
+    if (it == g_noalloc_ptr.end() || ctx == nullptr || it->second.ctx != ctx) {
         void *ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
             return MAXSIM_ERR_CUDA;
-        it = g_noalloc_ptr.emplace(dev, ptr).first;
+        if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return MAXSIM_ERR_CUDA;
+        it = g_noalloc_ptr.insert_or_assign(dev, ScratchAddress{ctx, ptr}).first;
     }
-    *out = it->second;
+    *out = it->second.ptr;
     return MAXSIM_OK;
 }
 

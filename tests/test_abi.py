@@ -125,14 +125,15 @@ def test_host_corpus_argument_errors_return_before_touching_the_device(lib):
     assert lib.maxsim_forward_host_workspace_size(1, 32, 3, 0, 64, 128, 0) == 0
 
 
-def test_run_case_driver_parses_without_a_gpu():
-    """The profiling driver imports and parses its arguments on a machine
-    without a GPU (it touches the device only when a case runs)."""
+def test_bench_case_mode_parses_without_a_gpu():
+    """bench.py's single-case mode (the command the profiles run) imports and
+    parses its arguments on a machine without a GPU (it touches the device
+    only when a case runs)."""
     import subprocess
     import sys
-    r = subprocess.run([sys.executable, "-m", "late_interaction_retrieval_maxsim_gb300.run_case", "--help"],
-                       cwd=ROOT, capture_output=True, text=True, timeout=300)
-    assert r.returncode == 0 and "chamfer" in r.stdout
+    r = subprocess.run([sys.executable, "bench.py", "--help"], cwd=ROOT, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0 and "chamfer" in r.stdout and "--case" in r.stdout
 
 
 def test_backward_rejects_misaligned_rows(lib):
@@ -147,3 +148,40 @@ def test_backward_rejects_misaligned_rows(lib):
         args = list(ok)
         args[pos] = vp(256 + 8)
         assert b(*args) == 1
+
+
+def test_noalloc_binding_checks_outputs_before_any_call(lib):
+    """maxsim_forward_noalloc writes into caller-provided outputs without
+    bounds checks, so the binding rejects a wrong shape, dtype or rank before
+    anything reaches the library (host tensors: the checks come before the
+    device check)."""
+    import torch
+
+    import late_interaction_retrieval_maxsim_gb300 as m
+    Q = torch.zeros((2, 40, 128), dtype=torch.float16)
+    D = torch.zeros((100, 128), dtype=torch.float16)
+    ql = torch.tensor([40, 3], dtype=torch.int32)
+    cu = torch.tensor([0, 60, 100], dtype=torch.int32)
+    ok_s = torch.zeros((2, 2))
+    cases = [
+        (dict(scores=torch.zeros((2, 1))), ValueError, "scores must have shape"),
+        (dict(scores=torch.zeros((2, 2), dtype=torch.float64)), TypeError, "scores must be"),
+        (dict(scores=ok_s, argmax=torch.zeros((2, 2, 39), dtype=torch.int32)), ValueError, "argmax must have shape"),
+        (dict(scores=ok_s, argmax=torch.zeros((2, 2, 40), dtype=torch.int64)), TypeError, "argmax must be"),
+        (dict(scores=ok_s, raw_scores=torch.zeros((1, 2), dtype=torch.int64)), ValueError, "raw_scores must have"),
+        (dict(scores=ok_s, raw_scores=torch.zeros((2, 2), dtype=torch.int32)), TypeError, "raw_scores must be"),
+        (dict(scores=torch.zeros((4, 2))[::2]), ValueError, "contiguous"),
+    ]
+    for kw, exc, msg in cases:
+        with pytest.raises(exc, match=msg):
+            m.maxsim_forward_noalloc(Q, ql, D, cu, **kw)
+    with pytest.raises(ValueError, match="Q must be"):
+        m.maxsim_forward_noalloc(Q[0], ql, D, cu, ok_s)
+    with pytest.raises(ValueError, match="Q must be"):
+        m.maxsim_forward_noalloc(Q, ql, D[:, :64], cu, ok_s)
+    # well-formed outputs get as far as the device check
+    with pytest.raises(ValueError, match="CUDA device"):
+        m.maxsim_forward_noalloc(Q, ql, D, cu, ok_s, argmax=torch.zeros((2, 2, 40), dtype=torch.int32))
+    # the allocating forward checks caller-provided outputs the same way
+    with pytest.raises(ValueError, match="scores must have shape"):
+        m.maxsim_forward(Q, ql, D, cu, scores=torch.zeros((3, 2)))

@@ -64,3 +64,16 @@ def test_no_kernel_and_errors():
         m.maxsim_forward_plan(-1, 32, 10, 100, sm_count=SMS)
     with pytest.raises(Exception):
         m.maxsim_forward_plan(1, 32, 10, 100, sm_count=0)
+
+
+def test_sizes_the_forward_rejects_are_rejected_here_too():
+    """The plan applies the forward's own size limits: a token count beyond
+    the kernels' 32-bit row range, or padded rows beyond int32, is an
+    argument error (status 1), as maxsim_forward reports it."""
+    with pytest.raises(m.MaxSimError) as e:
+        m.maxsim_forward_plan(1, 32, 10, 2**31 - 1, sm_count=SMS)
+    assert e.value.status == 1
+    with pytest.raises(m.MaxSimError) as e:
+        m.maxsim_forward_plan(2**26, 32, 10, 1000, sm_count=SMS)      # 2^31 padded rows
+    assert e.value.status == 1
+    assert plan(1, 32, 10, 2**31 - 1 - 256)["m_tiles"] == 1       # the largest token count accepted

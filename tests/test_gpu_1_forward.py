@@ -183,3 +183,63 @@ def test_training_forward_every_pair(ops):
     scores, argmax, _ = ops.maxsim_forward(x["Q"], x["q_lens"], x["D"], x["cu_seqlens"])
     assert ops.maxsim_device_status() == 0
     check_forward("bf16", x["Q"], x["q_lens"], x["D"], x["cu_seqlens"], scores, argmax)
+
+
+def _pow2_bf16_case(seed):
+    """BF16 inputs built from powers of two whose dot products are exact in
+    FP32: every query row is (2^-40, 2^-40, 2^-40, 0, ...).  "Peak" documents
+    hold the largest value 2^-77 = <q, (2^-37, 0, ...)> at column m and, at a
+    lower column p, its float predecessor 2^-77 - 2^-101 =
+    <q, (255 * 2^-45, 255 * 2^-53, 255 * 2^-61, 0, ...)> (three products of
+    255 * 2^-85, 2^-93, 2^-101: 24 bits in all); their other tokens are zero.
+    "Filler" documents between them hold 2^-70 everywhere, so a document
+    boundary inside a 32-column chunk meets a right-hand maximum in the
+    range of the fast indicator.  Exact ties and values make the argmax
+    unique: it must be m, bit for bit."""
+    rng = np.random.default_rng(seed)
+    q = np.zeros(128)
+    q[:3] = 2.0 ** -40
+    top = np.zeros(128)
+    top[0] = 2.0 ** -37
+    pred = np.zeros(128)
+    pred[:3] = [255 * 2.0 ** -45, 255 * 2.0 ** -53, 255 * 2.0 ** -61]
+    fill = np.zeros(128)
+    fill[0] = 2.0 ** -30
+    rows, lengths, expect = [], [], []
+    for k in range(120):
+        if k % 2 == 0:
+            ld = int(rng.integers(2, 90))
+            p = int(rng.integers(0, ld - 1))
+            m = p + 1 if rng.random() < 0.7 else int(rng.integers(p + 1, ld))
+            doc = np.zeros((ld, 128))
+            doc[p] = pred
+            doc[m] = top
+            expect.append(m)
+        else:
+            ld = int(rng.integers(1, 40))
+            doc = np.tile(fill, (ld, 1))
+            expect.append(0)
+        rows.append(doc)
+        lengths.append(ld)
+    D = torch.tensor(np.concatenate(rows), dtype=torch.bfloat16, device="cuda")
+    Q = torch.tensor(np.tile(q, (32, 1)), dtype=torch.bfloat16, device="cuda").view(1, 32, 128)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32, device="cuda")
+    ql = torch.tensor([32], dtype=torch.int32, device="cuda")
+    # the stored values are the intended powers of two
+    assert float(D[cu[0] + int(np.argmax(rows[0][:, 0] == 2.0 ** -37)), 0]) == 2.0 ** -37
+    return Q, ql, D, cu, np.array(expect)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_argmax_exact_at_tiny_power_of_two_maxima(ops, seed):
+    """A row maximum of exactly 2^-77 next to its float predecessor: the
+    exact argmax search must tell them apart (a fast-path bound one binade
+    too low reports the predecessor or a zero column).  Argmax bit-exact
+    against the oracle; scores exact (sums of powers of two)."""
+    Q, ql, D, cu, expect = _pow2_bf16_case(seed)
+    scores, argmax, _ = ops.maxsim_forward(Q, ql, D, cu)
+    assert ops.maxsim_device_status() == 0
+    ref = oracle.forward_bits("bf16", syn.bits_u16(Q), ql.cpu().numpy(), syn.bits_u16(D), cu.cpu().numpy())
+    assert np.array_equal(ref["argmax"][:, 0], expect)           # the construction is what it claims
+    assert np.array_equal(argmax[0].cpu().numpy(), ref["argmax"])
+    assert np.array_equal(scores[0].double().cpu().numpy(), ref["score"])

@@ -1,8 +1,10 @@
 """The INT8 variants of Flash-MaxSim §4.3.1 / §4.1 on the GPU against the
 oracle:
 
-  * INT8 with one scale per token: argmax bit-exact (both sides rank the
-    same binary32 products), scores within 1e-4 per query token;
+  * INT8 with one scale per token against the binary64 oracle: argmax equal
+    wherever the exact top-2 gap exceeds 2^-22 |max| (the kernel ranks the
+    products rounded once to binary32, a monotone rounding), a near-maximum
+    elsewhere; scores within 1e-4 per query token;
   * row-wise top-K: ids and values bit-exact;
   * the two-stage INT8 -> FP16 top-K scan: the stage-2 candidates exactly
     (the per-tensor INT8 stage is exact), the final ranking within the FP16
@@ -14,7 +16,7 @@ import torch
 
 import oracle
 from late_interaction_retrieval_maxsim_gb300 import synthetic as syn
-from maxsim_testlib import SCORE_TOL_PER_TOKEN, THREADS
+from maxsim_testlib import SCORE_TOL_PER_TOKEN, THREADS, check_int8_token
 
 pytestmark = pytest.mark.gpu
 
@@ -32,17 +34,8 @@ def _check_token(ops, Q8, qs, ql, D8, ds, cu):
     s, a = ops.maxsim_forward_int8_per_token(Q8, qs, ql, D8, ds, cu)
     torch.cuda.synchronize()
     assert ops.maxsim_device_status() == 0
-    ref = oracle.forward_i8_token(Q8.cpu().numpy(), qs.cpu().numpy(), ql.cpu().numpy(), D8.cpu().numpy(),
-                                  ds.cpu().numpy(), cu.cpu().numpy(), threads=THREADS)
-    n_q, lq = Q8.shape[:2]
-    a_ref = ref["argmax"].reshape(n_q, -1, lq)
-    assert np.array_equal(a.cpu().numpy(), a_ref)
-    s_ref = ref["score"].reshape(n_q, -1)
-    s_gpu = s.double().cpu().numpy()
-    neg = np.isneginf(s_ref)
-    assert np.array_equal(np.isneginf(s_gpu), neg)
-    lqs = np.maximum(ql.cpu().numpy(), 1)[:, None].repeat(s_ref.shape[1], 1)
-    assert np.all(np.abs(s_gpu[~neg] - s_ref[~neg]) <= SCORE_TOL_PER_TOKEN * lqs[~neg])
+    check_int8_token(Q8.cpu().numpy(), qs.cpu().numpy(), ql.cpu().numpy(), D8.cpu().numpy(), ds.cpu().numpy(),
+                     cu.cpu().numpy(), s.cpu().numpy(), a.cpu().numpy())
     # the value-only instantiation gives the same scores
     s2, _ = ops.maxsim_forward_int8_per_token(Q8, qs, ql, D8, ds, cu, with_argmax=False)
     assert torch.equal(s2, s)
@@ -195,8 +188,8 @@ def test_two_stage_rerank_fewer_documents_than_candidates(ops):
 
 def test_int8_per_token_full_size_sampled(ops):
     """The INT8 varlen workload at full size (32 x 32 queries vs 100,000
-    documents, Ld ~ U[32, 512]) with per-token scales: argmax bit-exact and
-    scores within tolerance on 40 sampled documents."""
+    documents, Ld ~ U[32, 512]) with per-token scales: argmax and scores
+    against the binary64 oracle on 40 sampled documents."""
     w = syn.WORKLOADS["int8_varlen"]
     cu = syn.cu_seqlens_from_lengths(syn.doc_lengths(w.n_docs, w.ld_lo, w.ld_hi, w.seed))
     total = int(cu[-1])
@@ -210,16 +203,12 @@ def test_int8_per_token_full_size_sampled(ops):
     rng = np.random.default_rng(3)
     docs = sorted(set(rng.integers(0, w.n_docs, 36).tolist()) | {0, 1, w.n_docs - 2, w.n_docs - 1})
     cu_h = cu.numpy()
-    pieces = [D8[int(cu_h[b]):int(cu_h[b + 1])] for b in docs]
-    sc = [ds[int(cu_h[b]):int(cu_h[b + 1])] for b in docs]
-    cu_sub = np.concatenate([[0], np.cumsum([p.shape[0] for p in pieces])]).astype(np.int32)
-    ref = oracle.forward_i8_token(Q8.cpu().numpy(), qs.cpu().numpy(), ql.cpu().numpy(),
-                                  torch.cat(pieces).cpu().numpy(), torch.cat(sc).cpu().numpy(), cu_sub,
-                                  threads=THREADS)
-    idx = torch.as_tensor(docs)
-    assert np.array_equal(a[:, idx].cpu().numpy(), ref["argmax"].reshape(w.n_q, len(docs), w.lq))
-    err = np.abs(s[:, idx].double().cpu().numpy() - ref["score"].reshape(w.n_q, len(docs)))
-    assert err.max() <= SCORE_TOL_PER_TOKEN * w.lq
+    D_sub = torch.cat([D8[int(cu_h[b]):int(cu_h[b + 1])] for b in docs])
+    ds_sub = torch.cat([ds[int(cu_h[b]):int(cu_h[b + 1])] for b in docs])
+    cu_sub = np.concatenate([[0], np.cumsum([int(cu_h[b + 1] - cu_h[b]) for b in docs])]).astype(np.int32)
+    idx = torch.as_tensor(docs, device="cuda")
+    check_int8_token(Q8.cpu().numpy(), qs.cpu().numpy(), ql.cpu().numpy(), D_sub.cpu().numpy(),
+                     ds_sub.cpu().numpy(), cu_sub, s[:, idx].cpu().numpy(), a[:, idx].cpu().numpy())
 
 
 def test_two_stage_rerank_full_size_sampled(ops):

@@ -1,12 +1,14 @@
 """Chamfer distance on the GPU (Flash-MaxSim §4.2 "Generalization to Chamfer
 Distance") against the oracle:
 
-  * nearest-neighbour distances and indices bit-exact (both sides rank the
-    same binary32 values, lowest index on ties), on ragged batches with
+  * nearest-neighbour distances and indices against the binary64 oracle:
+    distance within 2^-18 of the exact minimum (the kernel evaluates it in
+    binary32), index equal wherever the exact top-2 gap exceeds 2^-19 of the
+    second distance and a near-minimum elsewhere -- on ragged batches with
     empty sets and duplicated points, and on a large pair split into target
-    slices (sampled points);
-  * the per-item distance within 1e-6 relative (binary64 sums in another
-    order);
+    slices (sampled points); on integer coordinates both sides are exact and
+    every index and distance must match bit for bit (lowest index on ties);
+  * the per-item distance within 2^-17 relative;
   * the inverse CSR bit-exact; gradients within 1e-4 of the largest
     gradient; every output identical on a second run."""
 import numpy as np
@@ -14,8 +16,11 @@ import pytest
 import torch
 
 import oracle
+from maxsim_testlib import check_chamfer_nn
 
 pytestmark = pytest.mark.gpu
+
+CD_REL = 2.0 ** -17
 
 
 def _cloud(sizes, seed, dup_every=0):
@@ -28,19 +33,24 @@ def _cloud(sizes, seed, dup_every=0):
     return X.contiguous(), cu
 
 
-def _check_forward(ops, P, cu_p, Q, cu_q):
+def _check_forward(ops, P, cu_p, Q, cu_q, exact=False):
     cd, d_pq, a_pq, d_qp, a_qp = ops.maxsim_chamfer_forward(P, cu_p, Q, cu_q)
     torch.cuda.synchronize()
     assert ops.maxsim_device_status() == 0
-    ref = oracle.chamfer_forward(P.cpu().numpy(), cu_p.cpu().numpy(), Q.cpu().numpy(), cu_q.cpu().numpy())
-    assert np.array_equal(d_pq.cpu().numpy(), ref["dist_pq"])
-    assert np.array_equal(a_pq.cpu().numpy(), ref["arg_pq"])
-    assert np.array_equal(d_qp.cpu().numpy(), ref["dist_qp"])
-    assert np.array_equal(a_qp.cpu().numpy(), ref["arg_qp"])
+    Ph, Qh, cph, cqh = P.cpu().numpy(), Q.cpu().numpy(), cu_p.cpu().numpy(), cu_q.cpu().numpy()
+    ref = oracle.chamfer_forward(Ph, cph, Qh, cqh)
+    if exact:
+        assert np.array_equal(d_pq.double().cpu().numpy(), ref["dist_pq"])
+        assert np.array_equal(a_pq.cpu().numpy(), ref["arg_pq"])
+        assert np.array_equal(d_qp.double().cpu().numpy(), ref["dist_qp"])
+        assert np.array_equal(a_qp.cpu().numpy(), ref["arg_qp"])
+    else:
+        check_chamfer_nn(Ph, cph, Qh, cqh, d_pq.cpu().numpy(), a_pq.cpu().numpy())
+        check_chamfer_nn(Qh, cqh, Ph, cph, d_qp.cpu().numpy(), a_qp.cpu().numpy())
     got, want = cd.double().cpu().numpy(), ref["cd"]
     assert np.array_equal(np.isinf(got), np.isinf(want))
     fin = np.isfinite(want)
-    assert np.all(np.abs(got[fin] - want[fin]) <= 1e-6 * np.maximum(np.abs(want[fin]), 1e-30))
+    assert np.all(np.abs(got[fin] - want[fin]) <= CD_REL * np.abs(want[fin]))
     return cd, d_pq, a_pq, d_qp, a_qp
 
 
@@ -48,6 +58,17 @@ def test_forward_ragged_batch_with_empty_sets(ops):
     P, cu_p = _cloud([0, 1, 100, 1500, 5000, 37], seed=1, dup_every=7)
     Q, cu_q = _cloud([3, 0, 2000, 1500, 700, 1], seed=2, dup_every=5)
     _check_forward(ops, P, cu_p, Q, cu_q)
+
+
+def test_forward_integer_coordinates_bit_exact(ops):
+    """Integer coordinates: every distance is exact in binary32 and binary64,
+    ties are everywhere, and the lowest index must win them."""
+    g = torch.Generator("cuda").manual_seed(14)
+    P = torch.randint(-12, 13, (2600, 3), generator=g, device="cuda").float()
+    Q = torch.randint(-12, 13, (3100, 3), generator=g, device="cuda").float()
+    cu_p = torch.tensor([0, 100, 100, 2600], dtype=torch.int32, device="cuda")
+    cu_q = torch.tensor([0, 1, 1100, 3100], dtype=torch.int32, device="cuda")
+    _check_forward(ops, P, cu_p, Q, cu_q, exact=True)
 
 
 def test_forward_identical_sets(ops):
@@ -68,10 +89,8 @@ def test_forward_large_pair_sliced(ops):
     rng = np.random.default_rng(6)
     for S, T, d, a in ((P, Q, d_pq, a_pq), (Q, P, d_qp, a_qp)):
         idx = np.sort(rng.choice(S.shape[0], 400, replace=False))
-        Ss = S[torch.as_tensor(idx, device="cuda")].cpu().numpy()
-        rd, ra = oracle.chamfer_nn(Ss, [0, len(idx)], T.cpu().numpy(), [0, T.shape[0]])
-        assert np.array_equal(d.cpu().numpy()[idx], rd)
-        assert np.array_equal(a.cpu().numpy()[idx], ra)
+        check_chamfer_nn(S.cpu().numpy(), np.array([0, S.shape[0]], np.int32), T.cpu().numpy(),
+                         np.array([0, T.shape[0]], np.int32), d.cpu().numpy(), a.cpu().numpy(), rows=idx)
     ref_cd = float(d_pq.double().mean() + d_qp.double().mean())
     assert abs(float(cd[0]) - ref_cd) <= 1e-6 * ref_cd
 
