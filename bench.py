@@ -184,11 +184,27 @@ def _forward_launches(lq_max: int, int8: bool) -> int:
     return 1 + (1 if lq_pad > 32 else 0) + (1 if int8 else 0)
 
 
+def _l2_read_gbs(m, mib=48, passes=20):
+    """The SMs' read rate from L2: the library's plain-read probe over a
+    48 MiB buffer (L2-resident: the L2 holds 129 MB), one warm pass, then
+    `passes` timed passes (median of 5 launches)."""
+    import torch
+    stream = torch.cuda.current_stream()
+    buf = torch.zeros(mib << 20, dtype=torch.uint8, device="cuda")
+    sink = m.maxsim_probe_l2_read(buf, 1)
+    _, per = _time_loop(lambda: m.maxsim_probe_l2_read(buf, passes, sink=sink), 5, 2, stream)
+    gbs = buf.numel() * passes / (statistics.median(per) / 1e3) / 1e9
+    del buf, sink
+    return gbs
+
+
 def _extra_workloads(m, syn, rl, peaks):
     """Shorter timings of the other workloads (median of 20 CUDA-event reps)."""
     import torch
     out = {}
     stream = torch.cuda.current_stream()
+    l2_gbs = _l2_read_gbs(m)
+    out["l2_read_gbs"] = round(l2_gbs, 1)
     for name in ("colbert_varlen", "colbert_1q", "colpali", "train", "train_colpali", "int8_varlen"):
         w = syn.WORKLOADS[name]
         torch.cuda.empty_cache()
@@ -236,24 +252,49 @@ def _extra_workloads(m, syn, rl, peaks):
                                                            workspace=bws), 20, 3, stream)
             msb = statistics.median(perb)
 
-            # the training pair: the forward counts the CSR's sources, the
-            # backward skips its histogram pass
+            # one training step, forward then backward, on resident inputs
             def train_step():
-                m.maxsim_forward_with_counts(Q, ql, D, cu, scores=s, argmax=a, workspace=ws, backward_workspace=bws)
-                m.maxsim_backward_with_counts(g, a, Q, ql, D, cu, bws, dQ=dq, dD=dd)
+                m.maxsim_forward(Q, ql, D, cu, scores=s, argmax=a, workspace=ws)
+                m.maxsim_backward(g, a, Q, ql, D, cu, dQ=dq, dD=dd, workspace=bws)
             _, pers = _time_loop(train_step, 20, 3, stream)
-            _, perf = _time_loop(lambda: m.maxsim_forward_with_counts(Q, ql, D, cu, scores=s, argmax=a, workspace=ws,
-                                                                      backward_workspace=bws), 20, 3, stream)
+            # and end to end through the C ABI with host buffers: Q and D in,
+            # forward, the upstream gradient (here the synthetic contrastive
+            # one, computed from the scores on the device), backward, dQ and
+            # dD out
+            Qh, Dh = Q.cpu().pin_memory(), D.cpu().pin_memory()
+            dqh = torch.empty(dq.shape, dtype=torch.float32).pin_memory()
+            ddh = torch.empty(dd.shape, dtype=torch.float32).pin_memory()
+
+            def train_e2e():
+                Q.copy_(Qh, non_blocking=True)
+                D.copy_(Dh, non_blocking=True)
+                m.maxsim_forward(Q, ql, D, cu, scores=s, argmax=a, workspace=ws)
+                ge = torch.softmax(s / 0.05, dim=1)
+                ge[torch.arange(n, device="cuda"), torch.arange(n, device="cuda")] -= 1.0
+                m.maxsim_backward(ge, a, Q, ql, D, cu, dQ=dq, dD=dd, workspace=bws)
+                dqh.copy_(dq, non_blocking=True)
+                ddh.copy_(dd, non_blocking=True)
+            _, pere = _time_loop(train_e2e, 10, 3, stream)
             rec.update(train_step_ms=round(statistics.median(pers), 4),
-                       train_fwd_counting_ms=round(statistics.median(perf), 4),
-                       train_bwd_counted_ms=round(statistics.median(pers) - statistics.median(perf), 4))
+                       train_step_e2e_ms=round(statistics.median(pere), 4),
+                       train_e2e_h2d_bytes=Qh.numel() * Qh.element_size() + Dh.numel() * Dh.element_size(),
+                       train_e2e_d2h_bytes=dqh.numel() * 4 + ddh.numel() * 4)
+            del Qh, Dh, dqh, ddh
             bb = rl.backward_hbm_bytes(w.n_q, w.lq, w.n_docs, D.shape[0], int(ql.sum()) * w.n_docs)
             n_src = int(ql.sum()) * w.n_docs
+            gather = 2 * n_src * w.dim * 2
             rec.update(bwd_ms=round(msb, 4), step_ms=round(ms + msb, 4),
                        bwd_algorithmic_bytes=bb["total"],
-                       bwd_l2_gather_bytes=2 * n_src * w.dim * 2,
+                       bwd_l2_gather_bytes=gather,
                        bwd_gbs=bb["total"] / (msb / 1e3) / 1e9,
-                       bwd_frac_of_measured_hbm=bb["total"] / (msb / 1e3) / 1e9 / peaks["hbm_gbs"])
+                       bwd_frac_of_measured_hbm=bb["total"] / (msb / 1e3) / 1e9 / peaks["hbm_gbs"],
+                       # the gathers read 256-byte rows of an L2-resident Q / D: the
+                       # bound is the SMs' L2 read rate (measured above by the probe)
+                       bwd_roofline={"bound": "l2", "achieved": round((gather + bb["total"]) / (msb / 1e3) / 1e9, 1),
+                                     "peak": round(l2_gbs, 1), "unit": "GB/s",
+                                     "frac": round((gather + bb["total"]) / (msb / 1e3) / 1e9 / l2_gbs, 3),
+                                     "bytes": gather + bb["total"],
+                                     "peak_source": "maxsim_probe_l2_read, 48 MiB buffer, this run"})
         if m.maxsim_device_status() != 0:
             rec["device_status"] = "fault"
         out[name] = rec

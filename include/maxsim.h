@@ -314,19 +314,32 @@ maxsim_status_t maxsim_build_csr(const int32_t *argmax, const int32_t *q_lens, i
 
 /*
  * Training backward: Flash-MaxSim §4.2.1 Eqs. (2)-(3) via Alg. 3 -- the
- * argmax is inverted into the CSR above (kept in `workspace`), then
- *   dD[r, :]    = sum over the sources s of row r, in CSR order, of
+ * argmax is inverted into per-document lists of sources ordered as in the
+ * CSR above (each document's sources sorted by token in shared memory, in
+ * chunks of about 2,048 candidates, ascending source order within a token),
+ * then
+ *   dD[r, :]    = sum over the sources s = (q, b, i) of row r of
  *                 grad_scores[q, b] * Q[q, i, :]      (destination-owned,
  *                 one writer per row, no atomics; §4.2.3)
- *   dQ[q, i, :] = sum over b ascending of
+ *   dQ[q, i, :] = sum over b of
  *                 grad_scores[q, b] * D[cu_seqlens[b] + argmax[q, b, i], :]
- * both accumulated in FP32 in that fixed order.
+ * both accumulated in FP32 in a fixed order that depends only on the
+ * shapes and the argmax: each row's list is visited from a position derived
+ * from the row's index, wrapping around (rows that run together then read
+ * different parts of Q / D), its even and odd visits summed separately and
+ * the two sums added -- so the result is the same bit for bit on every run.
+ * dQ runs on a non-blocking stream the library keeps per device (created on
+ * the first backward on that device), forked from and joined back into
+ * `stream` with events, so it overlaps dD; the call is stream-ordered like
+ * every other.
  *   grad_scores FP32 [n_q, n_docs];  argmax as produced by maxsim_forward.
  *   dQ          FP32 [n_q, lq_max, dim], written in full (padding rows 0).
  *   dD          FP32 [total_d_tokens, dim], written in full (rows nobody
  *               selected are 0).
  *   Q, D, dQ and dD must start on a 16-byte boundary.
- * dtype: FP16 or BF16 (INT8 returns MAXSIM_ERR_UNSUPPORTED).
+ * dtype: FP16 or BF16 (INT8 returns MAXSIM_ERR_UNSUPPORTED).  At most
+ * 491,520 candidates per document (n_q * lq_max), else
+ * MAXSIM_ERR_UNSUPPORTED.
  */
 maxsim_status_t maxsim_backward(const float *grad_scores, const int32_t *argmax,
                                 const void *Q, const int32_t *q_lens, int32_t n_q, int32_t lq_max,
@@ -417,7 +430,10 @@ maxsim_status_t maxsim_chamfer_backward(const float *grad_cd, const float *P, co
  * maxsim_backward_workspace_size() bytes), which must then be handed,
  * unchanged, to maxsim_backward_with_counts together with this call's
  * argmax.  `workspace` is the forward's own scratch, as for maxsim_forward.
- * Scores and argmax are identical to maxsim_forward's.
+ * Scores and argmax are identical to maxsim_forward's.  The backward now
+ * sorts each document's sources itself in shared memory (see
+ * maxsim_backward) and needs no counts, so nothing is counted: this pair is
+ * maxsim_forward / maxsim_backward under the names of the training pair.
  */
 maxsim_status_t maxsim_forward_with_counts(const void *Q, const int32_t *q_lens, int32_t n_q, int32_t lq_max,
                                            const void *D, const int32_t *cu_seqlens, int32_t n_docs,
@@ -429,9 +445,8 @@ maxsim_status_t maxsim_forward_with_counts(const void *Q, const int32_t *q_lens,
 
 /*
  * maxsim_backward after maxsim_forward_with_counts: the same arguments and
- * results, with `workspace` the forward's `backward_workspace` (its counts
- * are used instead of a histogram pass over the argmax; the workspace is
- * consumed -- a second backward needs a new counting forward).
+ * results, with `workspace` the forward's `backward_workspace` (identical to
+ * maxsim_backward: see maxsim_forward_with_counts).
  */
 maxsim_status_t maxsim_backward_with_counts(const float *grad_scores, const int32_t *argmax,
                                             const void *Q, const int32_t *q_lens, int32_t n_q, int32_t lq_max,
@@ -463,6 +478,26 @@ maxsim_status_t maxsim_device_status(void *stream, int32_t clear, int32_t *code)
 maxsim_status_t maxsim_forward_plan(int32_t n_q, int32_t lq_max, int32_t n_docs, int64_t total_d_tokens,
                                     maxsim_dtype_t dtype, int32_t with_argmax, int32_t sm_count,
                                     int32_t *layout);
+
+/*
+ * A plain read of an L2-resident buffer, to measure the rate at which the
+ * SMs can read from L2 -- the bound of the backward's row gathers (each
+ * gradient row is a sum of 256-byte rows gathered from an L2-resident Q or
+ * D).  The pages have no counterpart; it is a measuring stick for the
+ * roofline of those kernels.  Enqueues one kernel of 2 CTAs per SM (at most
+ * 1024) that streams the `bytes` of `buf` `passes` times with 16-byte loads
+ * cached in L2 only, folding every word into sink[cta] (so the loads cannot be
+ * elided).  Time it with events on `stream`: rate = passes * bytes / time.
+ * For the rate to be L2's, `bytes` must fit in L2 with room to spare (on a
+ * GB300, 126 MB of L2: 32-64 MB) and a first pass should warm it.
+ *   buf     device, 16-byte aligned; bytes a multiple of 16, >= 16.
+ *   sink    device uint64 [1024], caller-owned, XOR-accumulated (any
+ *           initial contents).
+ * Returns MAXSIM_ERR_INVALID_ARGUMENT for a bad argument, MAXSIM_ERR_CUDA on a
+ * launch failure, else MAXSIM_OK.
+ */
+maxsim_status_t maxsim_probe_l2_read(const void *buf, size_t bytes, int32_t passes, uint64_t *sink,
+                                     void *stream);
 
 /*
  * Self-test of the kernels' failure path (no fault is involved): enqueues on

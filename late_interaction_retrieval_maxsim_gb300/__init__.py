@@ -20,8 +20,10 @@ Entry points (same names as the C ABI):
   maxsim_chamfer_forward / maxsim_chamfer_backward / maxsim_chamfer_build_csr
                    -- the Chamfer distance on the same skeleton
   maxsim_forward_with_counts / maxsim_backward_with_counts
-                   -- the training pair: the forward counts the backward's
-                      CSR sources while it produces the argmax
+                   -- the training pair under its earlier names (now the
+                      same as maxsim_forward / maxsim_backward: the backward
+                      sorts each document's sources itself)
+  maxsim_probe_l2_read -- a plain L2-resident read (the backward's roofline)
   maxsim_device_status, maxsim_forward_workspace_size,
   maxsim_backward_workspace_size, maxsim_abi_version
 """
@@ -37,7 +39,8 @@ __all__ = [
     "maxsim_forward_host_workspace_size", "maxsim_forward_int8_per_token", "maxsim_topk",
     "maxsim_rerank_two_stage", "maxsim_rerank_workspace_size", "maxsim_chamfer_forward",
     "maxsim_chamfer_backward", "maxsim_chamfer_build_csr", "maxsim_forward_with_counts",
-    "maxsim_backward_with_counts", "maxsim_selftest_bounded_wait", "maxsim_forward_plan", "MaxSimError",
+    "maxsim_backward_with_counts", "maxsim_selftest_bounded_wait", "maxsim_forward_plan", "maxsim_probe_l2_read",
+    "MaxSimError",
     "DTYPE_CODES",
 ]
 
@@ -123,6 +126,8 @@ def load_library():
     lib.maxsim_backward_with_counts.restype = ctypes.c_int
     lib.maxsim_device_status.argtypes = [vp, i32, ctypes.POINTER(i32)]
     lib.maxsim_device_status.restype = ctypes.c_int
+    lib.maxsim_probe_l2_read.argtypes = [vp, sz, i32, vp, vp]
+    lib.maxsim_probe_l2_read.restype = ctypes.c_int
     lib.maxsim_selftest_bounded_wait.argtypes = [ctypes.c_uint32, vp]
     lib.maxsim_selftest_bounded_wait.restype = ctypes.c_int
     lib.maxsim_forward_plan.argtypes = [i32, i32, i32, i64, ctypes.c_int, i32, i32, ctypes.POINTER(i32)]
@@ -639,8 +644,8 @@ def maxsim_backward(grad_scores, argmax, Q, q_lens, D, cu_seqlens, *, dQ=None, d
 def maxsim_forward_with_counts(Q, q_lens, D, cu_seqlens, *, scores=None, argmax=None, workspace=None,
                                backward_workspace=None, stream=None):
     """C: ``maxsim_forward_with_counts`` -- the training forward (FP16/BF16):
-    scores and argmax as ``maxsim_forward``, plus the backward's CSR source
-    counts in ``backward_workspace``.  Returns (scores, argmax,
+    scores and argmax as ``maxsim_forward`` (nothing is counted any more: the
+    backward sorts each document's sources itself).  Returns (scores, argmax,
     backward_workspace); pass the last two to ``maxsim_backward_with_counts``."""
     torch = _torch()
     lib = load_library()
@@ -674,9 +679,9 @@ def maxsim_forward_with_counts(Q, q_lens, D, cu_seqlens, *, scores=None, argmax=
 
 def maxsim_backward_with_counts(grad_scores, argmax, Q, q_lens, D, cu_seqlens, backward_workspace, *, dQ=None,
                                 dD=None, stream=None):
-    """C: ``maxsim_backward_with_counts`` -- ``maxsim_backward`` using the
-    counts ``maxsim_forward_with_counts`` left in ``backward_workspace``
-    (which this call consumes).  Returns (dQ, dD) float32."""
+    """C: ``maxsim_backward_with_counts`` -- ``maxsim_backward`` with the
+    workspace ``maxsim_forward_with_counts`` returned.  Returns (dQ, dD)
+    float32."""
     torch = _torch()
     lib = load_library()
     _require(grad_scores, "grad_scores", torch.float32)
@@ -715,6 +720,27 @@ def maxsim_forward_plan(n_q: int, lq_max: int, n_docs: int, total_d_tokens: int,
                                                           code, 1 if with_argmax else 0, int(sm_count), out))
     return {"m_tiles": out[0], "ctas_per_sm": out[1], "row_groups": out[2], "parts": out[3],
             "k_block_halves": bool(out[4])}
+
+
+PROBE_SINK_WORDS = 1024
+
+
+def maxsim_probe_l2_read(buf, passes: int, sink=None, stream=None):
+    """C: ``maxsim_probe_l2_read`` -- enqueue ``passes`` plain reads of the
+    device buffer ``buf`` (contiguous, 16-byte aligned, a multiple of 16
+    bytes); time them with events on ``stream``.  Returns the sink tensor
+    (uint64 words as int64 [1024])."""
+    torch = _torch()
+    lib = load_library()
+    _require(buf, "buf")
+    if sink is None:
+        sink = torch.zeros(PROBE_SINK_WORDS, dtype=torch.int64, device=buf.device)
+    _check_output(sink, "sink", (PROBE_SINK_WORDS,), torch.int64, buf.device)
+    nbytes = buf.numel() * buf.element_size()
+    with torch.cuda.device(buf.device):
+        st = lib.maxsim_probe_l2_read(_ptr(buf), nbytes, int(passes), _ptr(sink), _stream(stream))
+    _check("maxsim_probe_l2_read", st)
+    return sink
 
 
 def maxsim_selftest_bounded_wait(limit_us: int = 5000, stream=None) -> None:

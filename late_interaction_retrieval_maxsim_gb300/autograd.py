@@ -1,17 +1,13 @@
 """``torch.autograd`` entry point over the C ABI.
 
 "FLASH-MAXSIM: IO-Aware Fused Kernels for Late-Interaction Retrieval"
-(arXiv 2605.29517) §4.2.2 derives the inverse-grid CSR during the training
+(arXiv 2605.29517) §4.2.2 derives the inverse-grid map during the training
 step itself: the forward saves its argmax, and the backward turns it into dQ
 and dD without materialising the similarity tensor.  ``maxsim`` wraps exactly
-that: the forward keeps its argmax for the backward.  For queries of at most
-32 tokens it is ``maxsim_forward_with_counts`` (the CSR's source counts taken
-while the argmax is written) and the backward ``maxsim_backward_with_counts``,
-which then skips its counting pass; for longer queries the counting atomics
-cost the forward more than the backward saves (64 x 1024-token queries: 1.04
-against 0.98 ms forward, 6 us saved), so the plain ``maxsim_forward`` /
-``maxsim_backward`` pair runs.  Every step runs in the library's CUDA
-kernels; this module only routes tensors.
+that: ``maxsim_forward`` keeps its argmax for ``maxsim_backward``, which sorts
+each document's sources by token in shared memory and reduces them
+destination by destination.  Every step runs in the library's CUDA kernels;
+this module only routes tensors.
 
 Gradients are computed in FP32 by the kernels and returned in the inputs'
 dtype (autograd requires a gradient of its input's dtype); callers that need
@@ -21,11 +17,7 @@ from __future__ import annotations
 
 import torch
 
-from . import maxsim_backward, maxsim_backward_with_counts, maxsim_forward, maxsim_forward_with_counts
-
-# longest query (tokens) for which the training pair counts the CSR sources
-# in the forward
-COUNTED_MAX_LQ = 32
+from . import maxsim_backward, maxsim_forward
 
 
 class MaxSimFunction(torch.autograd.Function):
@@ -34,24 +26,14 @@ class MaxSimFunction(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, Q, D, q_lens, cu_seqlens):
-        if Q.shape[1] <= COUNTED_MAX_LQ:
-            scores, argmax, bws = maxsim_forward_with_counts(Q, q_lens, D, cu_seqlens)
-        else:
-            scores, argmax, _ = maxsim_forward(Q, q_lens, D, cu_seqlens)
-            bws = None
+        scores, argmax, _ = maxsim_forward(Q, q_lens, D, cu_seqlens)
         ctx.save_for_backward(Q, D, q_lens, cu_seqlens, argmax)
-        ctx.backward_workspace = bws   # the CSR source counts (or None); used up by one backward
         return scores
 
     @staticmethod
     def backward(ctx, grad_scores):
         Q, D, q_lens, cu_seqlens, argmax = ctx.saved_tensors
-        g = grad_scores.float().contiguous()
-        if ctx.backward_workspace is not None:
-            dQ, dD = maxsim_backward_with_counts(g, argmax, Q, q_lens, D, cu_seqlens, ctx.backward_workspace)
-            ctx.backward_workspace = None
-        else:   # no counts, or a second backward through the same graph: count from the argmax
-            dQ, dD = maxsim_backward(g, argmax, Q, q_lens, D, cu_seqlens)
+        dQ, dD = maxsim_backward(grad_scores.float().contiguous(), argmax, Q, q_lens, D, cu_seqlens)
         return (dQ.to(Q.dtype) if ctx.needs_input_grad[0] else None,
                 dD.to(D.dtype) if ctx.needs_input_grad[1] else None, None, None)
 

@@ -22,19 +22,21 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
+
 namespace maxsim {
 namespace {
 
 constexpr int kCsrWarps = 8;
 constexpr int kCsrThreads = 32 * kCsrWarps;
 constexpr int kCsrSmemBytes = 96 * 1024;   // per-warp histograms of one document chunk
-static_assert(kCsrSmemBytes / 4 == kCsrMaxDocTokens, "the forward's counts and the CSR agree on long documents");
+static_assert(kCsrSmemBytes / 4 == kCsrMaxDocTokens, "the shared histograms hold the longest document");
 // Documents of at most kCsrSmallDoc tokens (every workload here) run in a
 // first launch with small shared-memory footprints, so many CTAs share an SM;
 // longer ones run in a second launch with the full 96 KB.
 constexpr int kCsrSmallDoc = 4096;
 constexpr int kCsrSmallHistBytes = kCsrSmallDoc * 4;
-constexpr int kCsrSmallPlaceBytes = 24 * 1024;
+constexpr int kCsrSmallPlaceBytes = 32 * 1024;   // eight warps' histograms of a 1024-token document
 
 __device__ __forceinline__ bool valid_row(const BwdParams &p, int q, int i) {
     return i < p.q_lens[q];
@@ -101,26 +103,6 @@ __global__ void __launch_bounds__(256) csr_chunk_hist_kernel(BwdParams p, bool l
         int sum = 0;
         for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) sum += red[w];
         if (sum) atomicAdd(&p.doc_count[b], sum);
-    }
-}
-
-// Per document (one CTA), when the forward left the token counts:
-// doc_count[b] = the sum of the document's chunks * ld counts (a contiguous
-// range of chunk_cnt), in a fixed order.
-__global__ void __launch_bounds__(256) csr_doc_total_kernel(BwdParams p) {
-    const int b = blockIdx.x;
-    const int64_t lo = static_cast<int64_t>(p.chunks) * p.cu_seqlens[b];
-    const int64_t hi = static_cast<int64_t>(p.chunks) * p.cu_seqlens[b + 1];
-    int sum = 0;
-    for (int64_t k = lo + threadIdx.x; k < hi; k += blockDim.x) sum += p.chunk_cnt[k];
-    __shared__ int red[256 / 32];
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = sum;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int s = 0;
-        for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) s += red[w];
-        p.doc_count[b] = s;
     }
 }
 
@@ -293,95 +275,395 @@ __global__ void __launch_bounds__(kCsrThreads) csr_place_kernel(BwdParams p, boo
     }
 }
 
-__device__ __forceinline__ void load4(const void *base, int64_t row, int lane, bool bf16, float (&x)[4]) {
-    const uint2 u = reinterpret_cast<const uint2 *>(static_cast<const uint8_t *>(base) + row * 256)[lane];
-    if (bf16) {
-        const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162 *>(&u.x);
-        const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162 *>(&u.y);
-        x[0] = __low2float(lo); x[1] = __high2float(lo);
-        x[2] = __low2float(hi); x[3] = __high2float(hi);
-    } else {
-        const __half2 lo = *reinterpret_cast<const __half2 *>(&u.x);
-        const __half2 hi = *reinterpret_cast<const __half2 *>(&u.y);
-        x[0] = __low2float(lo); x[1] = __high2float(lo);
-        x[2] = __low2float(hi); x[3] = __high2float(hi);
+// ---------------------------------------------------------------- gathers
+//
+// Both gradients are sums of weighted 256-byte rows (128 FP16/BF16 values)
+// gathered from an L2-resident Q or D: dD row r = sum over its sources of
+// g * Q_row, dQ row (q, i) = sum over documents of g * D_row.  One warp owns
+// one output row; each half-warp gathers every other row of the list (half h
+// the positions j = h mod 2), each lane 16 bytes (8 values) of it, so one
+// warp instruction moves two rows, and the FMAs are packed two per
+// instruction: about 8 instructions per gathered row (ncu showed the
+// one-row-per-step form issuing 29 and the schedulers, not L2, setting the
+// pace).  At the end the half sums are added (half 0 + half 1).  The order is
+// fixed by the list, so the bits are the same on every run.
+
+__device__ __forceinline__ uint4 load_row16(const void *base, int64_t row, int c) {
+    return __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(base) + row * 256) + c);
+}
+
+// acc[k] += w * (values 2k, 2k+1 of the 8 in u), FP16 or BF16.
+__device__ __forceinline__ void fma8(uint4 u, float w, bool bf16, float2 (&acc)[4]) {
+    const float2 ww = make_float2(w, w);
+    const uint32_t v[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        float2 x;
+        if (bf16) {   // a bfloat16 is the upper half of a binary32
+            x.x = __uint_as_float(v[k] << 16);
+            x.y = __uint_as_float(v[k] & 0xffff0000u);
+        } else {
+            x = __half22float2(*reinterpret_cast<const __half2 *>(&v[k]));
+        }
+        acc[k] = ptx::fma2(ww, x, acc[k]);
     }
 }
 
-// dD (Eq. (3), Alg. 3 step 2): one warp owns destination row r, walks its
-// sources in CSR order accumulating g * Q_row in FP32, and writes the row
-// once (rows with no source are written as 0).
+// acc (this lane's 8 columns, 8 * (lane & 15) ..) += the sum, over the list
+// positions j = h (mod 2) of this lane's half-warp h in ascending order, of
+// w_j * X[row_j, :]; every lane l evaluates entry(base + l, base + l < n,
+// row, w) for each batch of 32 (the whole warp, so the entry may shuffle;
+// row < 0: no contribution), the next batch's entries while the current
+// batch's rows are gathered.  Whole warp, same n.
+template <typename Entry>
+__device__ __forceinline__ void warp_gather(const void *X, bool bf16, int n, Entry entry, float2 (&acc)[4]) {
+    const int lane = threadIdx.x & 31, h = lane >> 4, c = lane & 15;
+    if (n <= 0) return;
+    int rv = -1;
+    float wv = 0.f;
+    entry(lane, lane < n, rv, wv);
+    if (lane >= n) rv = -1;
+    for (int base = 0; base < n; base += 32) {
+        int nrv = -1;
+        float nwv = 0.f;
+        if (base + 32 < n) {
+            entry(base + 32 + lane, base + 32 + lane < n, nrv, nwv);
+            if (base + 32 + lane >= n) nrv = -1;
+        }
+        const int cnt = min(32, n - base);
+        for (int jb = 0; jb < cnt; jb += 4) {
+            int row[2];
+            float w[2];
+            uint4 raw[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int j = jb + 2 * u + h;   // <= 31
+                row[u] = __shfl_sync(0xffffffffu, rv, j);
+                w[u] = __shfl_sync(0xffffffffu, wv, j);
+                if (j >= cnt) row[u] = -1;
+                raw[u] = row[u] >= 0 ? load_row16(X, row[u], c) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+                if (row[u] >= 0) fma8(raw[u], w[u], bf16, acc);
+        }
+        rv = nrv;
+        wv = nwv;
+    }
+}
+
+// Adds the two half-warp sums (half 0 + half 1) and writes the 128-float row.
+__device__ __forceinline__ void warp_store_row(float *out_row, float2 (&acc)[4]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float ox = __shfl_xor_sync(0xffffffffu, acc[k].x, 16);
+        const float oy = __shfl_xor_sync(0xffffffffu, acc[k].y, 16);
+        acc[k] = (lane < 16) ? make_float2(acc[k].x + ox, acc[k].y + oy) : make_float2(ox + acc[k].x, oy + acc[k].y);
+    }
+    if (lane < 16) {
+        float4 *o = reinterpret_cast<float4 *>(out_row) + 2 * lane;
+        o[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
+        o[1] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
+    }
+}
+
+// The backward's own inverse map (the per-document reading of Alg. 3 step
+// 1: every source of document b lies in argmax[:, b, :]).  A document's
+// n_cand = n_q * lq_max candidates (flat order k = q * lq_max + i) are cut
+// into C <= 32 chunks; one CTA per (document, chunk) keeps its chunk's
+// tokens in shared memory and sorts the chunk's sources by token with a
+// stable counting sort (per-warp histograms, a prefix over (token, warp),
+// ranks within a warp from __match_any_sync), kSortWin tokens at a time.  It
+// writes the sorted candidates k (the source's Q row) to the fixed slots
+// [b * n_cand + k0, b * n_cand + k1) of `list`, and for every token r of the
+// document the bounds of its run there to row_start / row_end[r * C + c],
+// and each source's g[q, b] to the same slot of col_w.  No prefix over
+// documents is needed, and token r's runs read chunk after chunk give its sources in
+// ascending order: the CSR's row.
+constexpr int kSortWarps = 8;
+constexpr int kSortThreads = 32 * kSortWarps;
+constexpr int kSortQueries = 1024;   // queries of a chunk whose q_lens and g are staged
+
+// WIN tokens per window: 256 for documents of a few hundred tokens, 1024 for
+// page-length ones (each window rescans the chunk's tokens in shared memory).
+template <int WIN>
+size_t sort_smem_bytes(int chunk_len) {
+    // tokens, per-warp histograms, run starts, and the window's sorted output
+    // (candidate and weight) staged for coalesced writes
+    return static_cast<size_t>(chunk_len) * 4 * 3 + kSortWarps * WIN * 4 + (WIN + 1) * 4 + 16;
+}
+
+template <int WIN>
+__global__ void __launch_bounds__(kSortThreads) bwd_sort_kernel(BwdParams p) {
+    extern __shared__ __align__(16) uint8_t ssm[];
+    int32_t *tok = reinterpret_cast<int32_t *>(ssm);                 // [chunk_len]
+    int32_t *hist = tok + p.sort_chunk_len;                          // [W][WIN]
+    int32_t *start = hist + kSortWarps * WIN;                        // [WIN + 1]
+    int32_t *out_k = start + WIN + 1;                                // [chunk_len] the window's sorted sources
+    float *out_w = reinterpret_cast<float *>(out_k + p.sort_chunk_len);   // [chunk_len] their weights
+    __shared__ int32_t warp_tot[kSortWarps];
+    __shared__ int32_t s_ql[kSortQueries];
+    __shared__ float s_g[kSortQueries];
+    const int C = p.sort_chunks;
+    const int b = blockIdx.x / C, c = blockIdx.x - b * C;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = p.cu_seqlens[b];
+    const int ld = p.cu_seqlens[b + 1] - t0;
+    if (ld <= 0) return;
+    const int n_cand = p.n_q * p.lq_max;
+    const int k0 = min(n_cand, c * p.sort_chunk_len);
+    const int len = min(n_cand, k0 + p.sort_chunk_len) - k0;
+    int32_t *rs = p.row_start + static_cast<int64_t>(t0) * C + c;
+    int32_t *re = p.row_end + static_cast<int64_t>(t0) * C + c;
+    // q_lens and g[., b] of the chunk's queries, when they are few enough
+    const int q_lo = len > 0 ? query_of(p, k0) : 0;
+    const int n_qr = len > 0 ? query_of(p, k0 + len - 1) - q_lo + 1 : 0;
+    const bool staged = n_qr <= kSortQueries;
+    if (staged)
+        for (int qq = threadIdx.x; qq < n_qr; qq += kSortThreads) {
+            s_ql[qq] = p.q_lens[q_lo + qq];
+            s_g[qq] = p.grad[static_cast<int64_t>(q_lo + qq) * p.n_docs + b];
+        }
+    __syncthreads();
+    auto qlen_of = [&](int q) { return staged ? s_ql[q - q_lo] : p.q_lens[q]; };
+    auto g_of = [&](int q) { return staged ? s_g[q - q_lo] : p.grad[static_cast<int64_t>(q) * p.n_docs + b]; };
+
+    // 1. the chunk's candidates: the token each names, or -1 (four loads in
+    //    flight per thread)
+    for (int kb = threadIdx.x; kb < len; kb += 4 * kSortThreads) {
+        int a[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int kk = kb + u * kSortThreads;
+            a[u] = -1;
+            if (kk < len) {
+                const int k = k0 + kk;
+                const int q = query_of(p, k);
+                const int i = k - q * p.lq_max;
+                if (i < qlen_of(q)) a[u] = p.argmax[(static_cast<int64_t>(q) * p.n_docs + b) * p.lq_max + i];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int kk = kb + u * kSortThreads;
+            if (kk >= len) continue;
+            int v = a[u];
+            if (v < -1 || v >= ld) {
+                atomicCAS(p.status, 0, ptx::kStatusBadArgmax);
+                v = -1;
+            }
+            tok[kk] = v;
+        }
+    }
+    const int seg = ((len + kSortWarps - 1) / kSortWarps + 31) / 32 * 32;
+    const int s_lo = min(len, warp * seg), s_hi = min(len, s_lo + seg);
+    int32_t win_base = b * n_cand + k0;   // first slot of the current window's sources (< 2^31)
+
+    for (int w0 = 0; w0 < ld; w0 += WIN) {
+        const int win = min(WIN, ld - w0);
+        for (int k = threadIdx.x; k < kSortWarps * WIN; k += kSortThreads) hist[k] = 0;
+        __syncthreads();
+        // 2. per-warp histograms of the window's tokens
+        for (int kk = s_lo + lane; kk < s_hi; kk += 32) {
+            const int t = tok[kk] - w0;
+            if (t >= 0 && t < win) atomicAdd(&hist[warp * WIN + t], 1);
+        }
+        __syncthreads();
+        // 3. token totals -> exclusive scan -> each warp's first slot per
+        //    token (thread t holds tokens PER * t .. PER * t + PER - 1)
+        constexpr int PER = WIN / kSortThreads;
+        const int t = threadIdx.x;
+        int tot = 0;
+#pragma unroll
+        for (int e = 0; e < PER; ++e)
+#pragma unroll
+            for (int w = 0; w < kSortWarps; ++w) tot += hist[w * WIN + PER * t + e];
+        int x = tot;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+        }
+        if (lane == 31) warp_tot[warp] = x;
+        __syncthreads();
+        int run = x - tot;
+        for (int w = 0; w < warp; ++w) run += warp_tot[w];
+#pragma unroll
+        for (int e = 0; e < PER; ++e) {
+            const int tk = PER * t + e;
+            start[tk] = run;
+#pragma unroll
+            for (int w = 0; w < kSortWarps; ++w) {
+                const int v = hist[w * WIN + tk];
+                hist[w * WIN + tk] = run;
+                run += v;
+            }
+        }
+        if (t == kSortThreads - 1) start[WIN] = run;
+        __syncthreads();
+        for (int tk = t; tk < win; tk += kSortThreads) {
+            rs[static_cast<int64_t>(w0 + tk) * C] = win_base + start[tk];
+            re[static_cast<int64_t>(w0 + tk) * C] = win_base + start[tk + 1];
+        }
+        // 4. stable placement, 32 candidates at a time per warp
+        for (int kb = s_lo; kb < s_hi; kb += 32) {
+            const int kk = kb + lane;
+            const int tt = kk < s_hi ? tok[kk] - w0 : -1;
+            const bool mine = tt >= 0 && tt < win;
+            const int key = mine ? tt : (0x40000000 | lane);   // lanes without a source never match
+            const unsigned peers = __match_any_sync(0xffffffffu, key);
+            const int rank = __popc(peers & ((1u << lane) - 1u));
+            int pos = 0;
+            if (mine) pos = hist[warp * WIN + tt] + rank;
+            __syncwarp();
+            if (mine) {
+                out_k[pos] = k0 + kk;
+                out_w[pos] = g_of(query_of(p, k0 + kk));
+                if (rank == 0) hist[warp * WIN + tt] += __popc(peers);
+            }
+            __syncwarp();
+        }
+        __syncthreads();
+        // 5. the window's sorted sources to their slots, coalesced
+        const int n_win = start[WIN];
+        for (int e = threadIdx.x; e < n_win; e += kSortThreads) {
+            p.col_idx[win_base + e] = out_k[e];
+            p.col_w[win_base + e] = out_w[e];
+        }
+        win_base += n_win;
+        __syncthreads();
+    }
+}
+
+// The gathers of one output row start at a position derived from the row's
+// index and wrap around (a fixed order): rows that run at the same time then
+// read different parts of Q / D instead of all starting at the same
+// documents or queries and contending for the same L2 lines.
+__device__ __forceinline__ int rotation(int64_t row, int n) {
+    return n > 0 ? static_cast<int>((static_cast<uint64_t>(row) * 0x9E3779B1ull >> 7) % static_cast<uint64_t>(n)) : 0;
+}
+
+// dD (Eq. (3), Alg. 3 step 2): one warp owns destination row r and sums
+// g[q, b] * Q[q, i, :] over its sources, writing the row once (rows with no
+// source are 0).  Its sources are its runs read chunk after chunk
+// (ascending source order, the CSR's row) as one list of n entries: lane c <
+// C holds run c's bounds, and a position maps to its run by a prefix over the
+// run lengths.  The sum visits the list from position rotation(r, n),
+// wrapping around.
 __global__ void __launch_bounds__(256) grad_d_kernel(BwdParams p) {
-    const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int r = static_cast<int>((blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5);
+    if (r >= p.total_tokens) return;
     const int lane = threadIdx.x & 31;
-    if (warp_global >= p.total_tokens) return;
-    const int r = warp_global;
-    const int lo = p.row_ptr[r], hi = p.row_ptr[r + 1];
-    const int per_q = p.n_docs * p.lq_max;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int base = lo; base < hi; base += 32) {
-        const int n = min(32, hi - base);
-        int s = 0;
-        float gs = 0.f;
-        int qrow = 0;
-        if (lane < n) {
-            s = p.col_idx[base + lane];
-            const int q = s / per_q;
-            const int rem = s - q * per_q;
-            const int bb = rem / p.lq_max;
-            const int i = rem - bb * p.lq_max;
-            gs = p.grad[static_cast<int64_t>(q) * p.n_docs + bb];
-            qrow = q * p.lq_max + i;
-        }
-        for (int j = 0; j < n; ++j) {
-            const float g = __shfl_sync(0xffffffffu, gs, j);
-            const int row = __shfl_sync(0xffffffffu, qrow, j);
-            float x[4];
-            load4(p.Q, row, lane, p.bf16, x);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) acc[c] = fmaf(g, x[c], acc[c]);
-        }
+    const int C = p.sort_chunks;
+    int lo = 0, len = 0;
+    if (lane < C) {
+        lo = p.row_start[static_cast<int64_t>(r) * C + lane];
+        len = p.row_end[static_cast<int64_t>(r) * C + lane] - lo;
     }
-    reinterpret_cast<float4 *>(p.dD + static_cast<int64_t>(r) * 128)[lane] =
-        make_float4(acc[0], acc[1], acc[2], acc[3]);
+    int incl = len;   // inclusive prefix of the run lengths over lanes
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    const int n = __shfl_sync(0xffffffffu, incl, 31);
+    const int excl = incl - len;
+    const int first = rotation(r, n);
+    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    warp_gather(p.Q, p.bf16 != 0, n,
+                [&](int j, bool valid, int &row, float &w) {
+                    int pos = j + first;   // the list position visited j-th
+                    if (pos >= n) pos -= n;
+                    // the run holding pos: the number of runs whose end is <= pos,
+                    // found by a binary search over the lanes' inclusive ends
+                    int run = 0;
+#pragma unroll
+                    for (int step = 16; step > 0; step >>= 1)
+                        if (__shfl_sync(0xffffffffu, incl, run + step - 1) <= pos) run += step;
+                    run = min(run, 31);
+                    const int at = __shfl_sync(0xffffffffu, lo, run) + pos - __shfl_sync(0xffffffffu, excl, run);
+                    if (!valid) return;
+                    row = p.col_idx[at];
+                    w = p.col_w[at];
+                },
+                acc);
+    warp_store_row(p.dD + static_cast<int64_t>(r) * 128, acc);
 }
 
-// dQ (Eq. (2), Alg. 3 step 3): one warp owns query row (q, i) and gathers
-// g[q, b] * D[cu[b] + t*] over documents b in ascending order.
-__global__ void __launch_bounds__(256) grad_q_kernel(BwdParams p) {
-    const int64_t warp_global = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (warp_global >= static_cast<int64_t>(p.n_q) * p.lq_max) return;
-    const int q = static_cast<int>(warp_global / p.lq_max);
-    const int i = static_cast<int>(warp_global - static_cast<int64_t>(q) * p.lq_max);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (i < p.q_lens[q]) {
-        for (int b0 = 0; b0 < p.n_docs; b0 += 32) {
-            const int n = min(32, p.n_docs - b0);
-            int trow = -1;
-            float gs = 0.f;
-            if (lane < n) {
-                const int b = b0 + lane;
-                const int t = p.argmax[(static_cast<int64_t>(q) * p.n_docs + b) * p.lq_max + i];
-                const int lo = p.cu_seqlens[b];
-                const int ld = p.cu_seqlens[b + 1] - lo;
-                if (t >= 0 && t < ld) {
-                    trow = lo + t;
-                    gs = p.grad[static_cast<int64_t>(q) * p.n_docs + b];
-                }
-            }
-            for (int j = 0; j < n; ++j) {
-                const int row = __shfl_sync(0xffffffffu, trow, j);
-                const float g = __shfl_sync(0xffffffffu, gs, j);
-                if (row < 0) continue;
-                float x[4];
-                load4(p.D, row, lane, p.bf16, x);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) acc[c] = fmaf(g, x[c], acc[c]);
-            }
+// dQ's lists: rowidx[(q * lq_max + i) * n_docs + b] = cu[b] + argmax[q, b, i]
+// (the D row query row (q, i) selected in document b), -1 for none -- the
+// argmax transposed so that a row's list is contiguous.  One CTA moves a
+// 32 x 32 tile (documents x query tokens) of one query through shared memory.
+__global__ void __launch_bounds__(256) dq_rows_kernel(BwdParams p, int32_t *rowidx) {
+    __shared__ int32_t tile[32][33];
+    const int tiles_b = (p.n_docs + 31) / 32, tiles_i = (p.lq_max + 31) / 32;
+    const int q = blockIdx.x / (tiles_b * tiles_i);
+    const int rem = blockIdx.x - q * tiles_b * tiles_i;
+    const int b0 = (rem / tiles_i) * 32, i0 = (rem % tiles_i) * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int qlen = p.q_lens[q];
+    for (int bb = ty; bb < 32; bb += 8) {   // read: query tokens contiguous
+        const int b = b0 + bb, i = i0 + tx;
+        int v = -1;
+        if (b < p.n_docs && i < p.lq_max && i < qlen) {
+            const int a = p.argmax[(static_cast<int64_t>(q) * p.n_docs + b) * p.lq_max + i];
+            const int lo = p.cu_seqlens[b];
+            if (a >= 0 && a < p.cu_seqlens[b + 1] - lo) v = lo + a;
         }
+        tile[bb][tx] = v;
     }
-    reinterpret_cast<float4 *>(p.dQ + warp_global * 128)[lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    __syncthreads();
+    for (int ii = ty; ii < 32; ii += 8) {   // write: documents contiguous
+        const int b = b0 + tx, i = i0 + ii;
+        if (b < p.n_docs && i < p.lq_max)
+            rowidx[(static_cast<int64_t>(q) * p.lq_max + i) * p.n_docs + b] = tile[tx][ii];
+    }
+}
+
+// dQ (Eq. (2), Alg. 3 step 3): one warp owns query row (q, i) and sums
+// g[q, b] * D[rowidx[b]] over the documents, its list visited from
+// rotation(row, n_docs) upward, wrapping around.
+__global__ void __launch_bounds__(256, 8) grad_q_kernel(BwdParams p, const int32_t *rowidx) {
+    const int64_t R = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
+    if (R >= static_cast<int64_t>(p.n_q) * p.lq_max) return;
+    const int q = query_of(p, static_cast<int>(R));
+    const int i = static_cast<int>(R) - q * p.lq_max;
+    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    if (i < p.q_lens[q]) {
+        const int first = rotation(R, p.n_docs);
+        const int32_t *rows = rowidx + R * p.n_docs;
+        const float *g = p.grad + static_cast<int64_t>(q) * p.n_docs;
+        warp_gather(p.D, p.bf16 != 0, p.n_docs,
+                    [&](int j, bool valid, int &row, float &w) {
+                        if (!valid) return;
+                        int b = j + first;
+                        if (b >= p.n_docs) b -= p.n_docs;
+                        row = rows[b];
+                        w = g[b];
+                    },
+                    acc);
+    }
+    warp_store_row(p.dQ + R * 128, acc);
+}
+
+// A plain L2-resident read: every CTA streams the buffer's 16-byte words
+// `passes` times (grid-stride), folding them into one word per thread so the
+// loads cannot be dropped; sink[blockIdx.x] receives the fold.
+__global__ void __launch_bounds__(512) l2_read_probe_kernel(const uint4 *buf, int64_t n16, int passes,
+                                                            unsigned long long *sink) {
+    uint32_t f = 0;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int pass = 0; pass < passes; ++pass)
+        for (int64_t k = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; k < n16; k += 4 * stride) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = k + u * stride < n16 ? __ldcg(buf + k + u * stride) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) f ^= v[u].x ^ v[u].y ^ v[u].z ^ v[u].w;
+        }
+    for (int off = 16; off > 0; off >>= 1) f ^= __shfl_xor_sync(0xffffffffu, f, off);
+    if ((threadIdx.x & 31) == 0) atomicXor(sink + blockIdx.x, static_cast<unsigned long long>(f));
 }
 
 }  // namespace
@@ -399,7 +681,7 @@ int csr_chunks(int32_t n_q, int32_t lq_max, int32_t n_docs) {
     return static_cast<int>(c < 1 ? 1 : c);
 }
 
-cudaError_t launch_build_csr(const BwdParams &p, cudaStream_t stream, bool counts_ready) {
+cudaError_t launch_build_csr(const BwdParams &p, cudaStream_t stream) {
     if (p.n_docs == 0) {
         return cudaMemsetAsync(p.row_ptr, 0, sizeof(int32_t) * (p.total_tokens + 1), stream);
     }
@@ -407,18 +689,12 @@ cudaError_t launch_build_csr(const BwdParams &p, cudaStream_t stream, bool count
     const unsigned grid = static_cast<unsigned>(p.n_docs) * p.chunks;
     // a document longer than kCsrSmallDoc needs a second, large-footprint launch
     const bool any_large = p.total_tokens > kCsrSmallDoc;
-    if (!counts_ready) {
-        if ((e = cudaMemsetAsync(p.doc_count, 0, sizeof(int32_t) * (p.n_docs + 1), stream)) != cudaSuccess)
-            return e;
-        if ((e = cudaFuncSetAttribute(csr_chunk_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      kCsrSmemBytes)) != cudaSuccess)
-            return e;
-        csr_chunk_hist_kernel<<<grid, 256, kCsrSmallHistBytes, stream>>>(p, false);
-        if (any_large) csr_chunk_hist_kernel<<<grid, 256, kCsrSmemBytes, stream>>>(p, true);
-    }
-    // (with counts from the forward, documents too long for the CSR are
-    // reported by csr_place_kernel)
-    if (counts_ready) csr_doc_total_kernel<<<p.n_docs, 256, 0, stream>>>(p);
+    if ((e = cudaMemsetAsync(p.doc_count, 0, sizeof(int32_t) * (p.n_docs + 1), stream)) != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(csr_chunk_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kCsrSmemBytes)) != cudaSuccess)
+        return e;
+    csr_chunk_hist_kernel<<<grid, 256, kCsrSmallHistBytes, stream>>>(p, false);
+    if (any_large) csr_chunk_hist_kernel<<<grid, 256, kCsrSmemBytes, stream>>>(p, true);
     csr_doc_scan_kernel<<<1, 1024, 0, stream>>>(p);
     csr_token_scan_kernel<<<p.n_docs, 256, 0, stream>>>(p);
     if ((e = cudaFuncSetAttribute(csr_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -429,17 +705,55 @@ cudaError_t launch_build_csr(const BwdParams &p, cudaStream_t stream, bool count
     return cudaGetLastError();
 }
 
-cudaError_t launch_grad_d(const BwdParams &p, cudaStream_t stream) {
-    if (p.total_tokens == 0) return cudaSuccess;
+int sort_chunks(int32_t n_q, int32_t lq_max) {
+    const int64_t n_cand = static_cast<int64_t>(n_q) * lq_max;
+    const int64_t c = (n_cand + kSortChunkTarget - 1) / kSortChunkTarget;
+    return static_cast<int>(c < 1 ? 1 : (c > kSortMaxChunks ? kSortMaxChunks : c));
+}
+
+static_assert(kSortMaxChunkLen * 12 + kSortWarps * 1024 * 4 + 1025 * 4 + 16 + 2 * 4096 + 64 <= 227 * 1024,
+              "the largest sort chunk fits one CTA's shared memory");
+
+template <int WIN>
+cudaError_t launch_sort(const BwdParams &p, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(bwd_sort_kernel<WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(sort_smem_bytes<WIN>(kSortMaxChunkLen)));
+    if (e != cudaSuccess) return e;
+    bwd_sort_kernel<WIN><<<static_cast<unsigned>(p.n_docs) * p.sort_chunks, kSortThreads,
+                           sort_smem_bytes<WIN>(p.sort_chunk_len), stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sort_and_grad_d(const BwdParams &p, cudaStream_t stream) {
+    if (p.total_tokens == 0 || p.n_docs == 0) return cudaSuccess;
+    if (static_cast<int64_t>(p.n_q) * p.lq_max == 0)   // no source: every row is 0
+        return cudaMemsetAsync(p.dD, 0, sizeof(float) * 128 * static_cast<size_t>(p.total_tokens), stream);
+    // windows of 1024 tokens when documents average more than 256
+    const bool long_docs = p.total_tokens > 256 * static_cast<int64_t>(p.n_docs);
+    cudaError_t e = long_docs ? launch_sort<1024>(p, stream) : launch_sort<256>(p, stream);
+    if (e != cudaSuccess) return e;
     const int64_t threads = static_cast<int64_t>(p.total_tokens) * 32;
     grad_d_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_grad_q(const BwdParams &p, cudaStream_t stream) {
+cudaError_t launch_grad_q(const BwdParams &p, int32_t *rowidx, cudaStream_t stream) {
     const int64_t rows = static_cast<int64_t>(p.n_q) * p.lq_max;
     if (rows == 0) return cudaSuccess;
-    grad_q_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, stream>>>(p);
+    if (p.n_docs > 0) {
+        const int64_t tiles = static_cast<int64_t>(p.n_q) * ((p.n_docs + 31) / 32) * ((p.lq_max + 31) / 32);
+        dq_rows_kernel<<<static_cast<unsigned>(tiles), 256, 0, stream>>>(p, rowidx);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    grad_q_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, stream>>>(p, rowidx);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_l2_read_probe(const void *buf, size_t bytes, int passes, unsigned long long *sink, int ctas,
+                                 cudaStream_t stream) {
+    l2_read_probe_kernel<<<ctas, 512, 0, stream>>>(static_cast<const uint4 *>(buf),
+                                                   static_cast<int64_t>(bytes / 16), passes, sink);
     return cudaGetLastError();
 }
 

@@ -282,9 +282,8 @@ __device__ __forceinline__ void fold_split(const uint32_t (&r)[32], int c0, int 
 // row and the (partial) score.  DB double-buffers the TMEM reads.  INT8 sums
 // the (integer) maxima in int64; SCALE multiplies each column by its
 // document token's scale before the maximum and the row maximum by the
-// query token's scale, then sums in FP32.  COUNT (training) also counts the
-// backward's CSR sources as the argmax is written.
-template <bool ARGMAX, bool INT8, bool SCALE, bool DB, bool COUNT, typename SlotOf, typename Release>
+// query token's scale, then sums in FP32.
+template <bool ARGMAX, bool INT8, bool SCALE, bool DB, typename SlotOf, typename Release>
 __device__ __forceinline__ void epilogue_warp(const FwdParams &p, int rho_warp, int64_t rows_total,
                                               uint32_t tmem_base, int qd, int b_begin, int b_end,
                                               int t_begin, int t_end, int n_tiles, uint64_t *t_full,
@@ -298,9 +297,6 @@ __device__ __forceinline__ void epilogue_warp(const FwdParams &p, int rho_warp, 
     const bool row_valid = q < p.n_q && i < p.lq_max;
     const int qlen = (q < p.n_q) ? p.q_lens[q] : 0;
     const bool active = row_valid && i < qlen;
-    // training mode: the CSR chunk of this row's sources (chunks of n_q * lq_max
-    // candidates in flat order q * lq_max + i)
-    [[maybe_unused]] const int csr_chunk = (COUNT && row_valid) ? (q * p.lq_max + i) / p.csr_chunk_len : 0;
     const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
     [[maybe_unused]] const float q_scale = (SCALE && active) ? p.q_tok_scale[q * p.lq_max + i] : 0.0f;
 
@@ -354,15 +350,6 @@ __device__ __forceinline__ void epilogue_warp(const FwdParams &p, int rho_warp, 
         if (ARGMAX && row_valid)
             p.argmax[(static_cast<int64_t>(q) * p.ld_out + b) * p.lq_max + i] =
                 (active && a >= 0) ? a - doc_lo : -1;
-        if constexpr (ARGMAX && COUNT) {
-            // training mode: count this source for the backward's inverse map
-            // (integer atomics: the counts do not depend on their order)
-            const int ldb = doc_hi - doc_lo;
-            const bool src = active && a >= 0 && ldb <= kCsrMaxDocTokens;
-            if (src)
-                atomicAdd(p.csr_cnt + static_cast<int64_t>(p.csr_chunks) * doc_lo +
-                              static_cast<int64_t>(csr_chunk) * ldb + (a - doc_lo), 1);
-        }
         if (INT8) {
             const bool empty_doc = doc_hi == doc_lo;
             long long c = (active && !empty_doc) ? static_cast<long long>(m) : 0ll;

@@ -114,7 +114,7 @@ __device__ __forceinline__ uint2 widen_i8x4(uint32_t w) {
     return make_uint2(*reinterpret_cast<uint32_t *>(&l), *reinterpret_cast<uint32_t *>(&h));
 }
 
-template <int NMT, bool ARGMAX, bool INT8, bool SCALE, bool COUNT>
+template <int NMT, bool ARGMAX, bool INT8, bool SCALE>
 __global__ void __launch_bounds__(Cfg<NMT, INT8>::kThreads, Cfg<NMT, INT8>::kCtasPerSm)
 maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmD,
                   const FwdParams p) {
@@ -342,7 +342,7 @@ maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         const int mt = (warp - C::kFirstEpiWarp) >> 2;
         const int qd = warp & 3;  // TMEM lane quarter this warp may access
         if (mt < n_mt) {
-            epilogue_warp<ARGMAX, INT8 && !SCALE, SCALE, C::kDoubleBuffer, COUNT>(
+            epilogue_warp<ARGMAX, INT8 && !SCALE, SCALE, C::kDoubleBuffer>(
                 p, row0 + mt * 128 + qd * 32, rows_total, tmem_base, qd, b_begin, b_end, t_begin, t_end,
                 n_tiles, ctl->t_full, ctl->scale_buf[warp - C::kFirstEpiWarp],
                 [&](int j) { return make_int2(mt + NMT * (j % (C::kSlots / NMT)), j / (C::kSlots / NMT)); },
@@ -403,24 +403,24 @@ __global__ void int8_to_f16_kernel(const int8_t *__restrict__ src, __half *__res
         dst[k] = __int2half_rn(static_cast<int>(src[k]));
 }
 
-template <int NMT, bool ARGMAX, bool INT8, bool SCALE, bool COUNT = false>
+template <int NMT, bool ARGMAX, bool INT8, bool SCALE>
 cudaError_t launch_one(const CUtensorMap &tmQ, const CUtensorMap &tmD, const FwdParams &p,
                        cudaStream_t stream) {
     using C = Cfg<NMT, INT8>;
-    auto kern = maxsim_fwd_kernel<NMT, ARGMAX, INT8, SCALE, COUNT>;
+    auto kern = maxsim_fwd_kernel<NMT, ARGMAX, INT8, SCALE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     kern<<<p.groups * p.parts, C::kThreads, C::kSmem, stream>>>(tmQ, tmD, p);
     return cudaGetLastError();
 }
 
-template <bool ARGMAX, bool INT8, bool SCALE, bool COUNT = false>
+template <bool ARGMAX, bool INT8, bool SCALE>
 cudaError_t launch_nmt(int nmt, const CUtensorMap &tmQ, const CUtensorMap &tmD, const FwdParams &p,
                        cudaStream_t stream) {
     switch (nmt) {
-        case 1: return launch_one<1, ARGMAX, INT8, SCALE, COUNT>(tmQ, tmD, p, stream);
-        case 2: return launch_one<2, ARGMAX, INT8, SCALE, COUNT>(tmQ, tmD, p, stream);
-        default: return launch_one<4, ARGMAX, INT8, SCALE, COUNT>(tmQ, tmD, p, stream);
+        case 1: return launch_one<1, ARGMAX, INT8, SCALE>(tmQ, tmD, p, stream);
+        case 2: return launch_one<2, ARGMAX, INT8, SCALE>(tmQ, tmD, p, stream);
+        default: return launch_one<4, ARGMAX, INT8, SCALE>(tmQ, tmD, p, stream);
     }
 }
 
@@ -460,7 +460,6 @@ cudaError_t launch_forward(const CUtensorMap &tmQ, const CUtensorMap &tmD, const
             return with_argmax ? launch_nmt<true, true, true>(nmt, tmQ, tmD, p, stream)
                                : launch_nmt<false, true, true>(nmt, tmQ, tmD, p, stream);
         default:
-            if (with_argmax && p.csr_cnt != nullptr) return launch_nmt<true, false, false, true>(nmt, tmQ, tmD, p, stream);
             return with_argmax ? launch_nmt<true, false, false>(nmt, tmQ, tmD, p, stream)
                                : launch_nmt<false, false, false>(nmt, tmQ, tmD, p, stream);
     }

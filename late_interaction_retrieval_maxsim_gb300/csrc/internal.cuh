@@ -23,8 +23,6 @@ struct FwdParams {
     int32_t *argmax;     // [n_q, ld_out, lq_max] or null
     const float *q_tok_scale;  // INT8 per-token mode: [n_q, lq_max] query-token scales
     const float *d_tok_scale;  // INT8 per-token mode: [total_tokens] document-token scales
-    int32_t *csr_cnt;          // training mode (or null): per-(document, chunk, token) source counts
-    int32_t csr_chunks, csr_chunk_len;
     int32_t *status;     // device status word
     int32_t n_q, lq_max, lq_pad, n_docs;
     int32_t total_tokens;
@@ -119,6 +117,10 @@ struct BwdParams {
     int32_t *col_idx;        // [n_q * n_docs * lq_max]
     int32_t *doc_count;      // [n_docs + 1] scratch: sources per document, then offsets
     int32_t *chunk_cnt;      // [chunks * total] scratch: per-chunk token counts, then first slots
+    int32_t *row_start;      // [total * sort_chunks]: first col_idx slot of (token, chunk)'s sources
+    int32_t *row_end;        // [total * sort_chunks]: one past the last
+    float *col_w;            // [n_docs * n_q * lq_max]: the backward's sorted sources' g[q, b]
+    int32_t sort_chunks, sort_chunk_len;   // candidate chunks per document of the backward's sort
     int32_t *status;
     int32_t n_q, lq_max, n_docs, total_tokens;
     int32_t chunks;          // candidate chunks per document (csr_chunks)
@@ -139,10 +141,26 @@ int csr_chunks(int32_t n_q, int32_t lq_max, int32_t n_docs);
 // Longest document the CSR build handles (its shared-memory histograms);
 // longer ones get empty rows and a status code.
 constexpr int kCsrMaxDocTokens = 24 * 1024;
-// counts_ready: doc_count and chunk_cnt were filled by the forward (training
-// mode), so the histogram pass is skipped.
-cudaError_t launch_build_csr(const BwdParams &p, cudaStream_t stream, bool counts_ready = false);
-cudaError_t launch_grad_d(const BwdParams &p, cudaStream_t stream);
-cudaError_t launch_grad_q(const BwdParams &p, cudaStream_t stream);
+// The exact CSR (maxsim_build_csr): chunked per-document counting sort.
+cudaError_t launch_build_csr(const BwdParams &p, cudaStream_t stream);
+// dQ: the argmax transposed into per-row lists of D rows (rowidx, n_q *
+// lq_max * n_docs int32 of scratch), then one warp per dQ row.
+cudaError_t launch_grad_q(const BwdParams &p, int32_t *rowidx, cudaStream_t stream);
+// The backward's inverse map and dD: each document's n_q * lq_max candidates
+// in C = sort_chunks() chunks (about kSortChunkTarget each, at most
+// kSortMaxChunks chunks of at most kSortMaxChunkLen), sorted per (document,
+// chunk) in shared memory into fixed slots of col_idx (their g[q, b] in the
+// same slots of col_w), with per-(token, chunk) run bounds in row_start /
+// row_end; then one warp per dD row.
+constexpr int kSortChunkTarget = 2048;
+constexpr int kSortMaxChunks = 32;
+constexpr int kSortMaxChunkLen = 15360;   // tokens and staged output: 180 KB of shared memory
+constexpr int64_t kBackwardMaxCandidates = int64_t{kSortMaxChunks} * kSortMaxChunkLen;
+int sort_chunks(int32_t n_q, int32_t lq_max);
+cudaError_t launch_sort_and_grad_d(const BwdParams &p, cudaStream_t stream);
+// Streams `bytes` of `buf` (16-byte aligned, a multiple of 16) `passes` times
+// with `ctas` CTAs of 512 threads, folding the words into sink[0 .. ctas).
+cudaError_t launch_l2_read_probe(const void *buf, size_t bytes, int passes, unsigned long long *sink, int ctas,
+                                 cudaStream_t stream);
 
 }  // namespace maxsim

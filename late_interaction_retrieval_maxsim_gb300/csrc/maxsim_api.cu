@@ -26,6 +26,7 @@ namespace {
 
 constexpr int kDim = 128;
 constexpr size_t kAlign = 256;
+constexpr int kProbeSinkWords = 1024;   // the L2 probe's sink: one word per CTA
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -67,6 +68,33 @@ maxsim_status_t device_info(DeviceInfo *out) {
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// A non-blocking stream per device (and the two events that fork work onto
+// it from a caller's stream and join it back), created on first use with the
+// device current and kept for the life of the process.  g_side_mu serialises
+// the fork / launch / join sequences of concurrent callers.
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;
+std::unordered_map<int, SideStream> g_side;
+
+maxsim_status_t side_stream(SideStream *out) {   // caller holds g_side_mu
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MAXSIM_ERR_CUDA;
+    auto it = g_side.find(dev);
+    if (it == g_side.end()) {
+        SideStream s;
+        if (cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking) != cudaSuccess) return MAXSIM_ERR_CUDA;
+        if (cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess)
+            return MAXSIM_ERR_CUDA;
+        it = g_side.emplace(dev, s).first;
+    }
+    *out = it->second;
+    return MAXSIM_OK;
+}
 
 int lq_padded(int lq_max) {
     if (lq_max <= 32) {
@@ -133,8 +161,12 @@ FwdLayout forward_layout(int32_t n_q, int32_t lq_max, int32_t n_docs, maxsim_dty
     return l;
 }
 
+// Backward / CSR scratch: the CSR (row_ptr, col_idx) and its per-document
+// and per-chunk counts; the backward's own sort fills col_idx in
+// per-(document, chunk) slots instead, with the sources' weights in a second
+// array of the same size and the runs' bounds.
 struct BwdLayout {
-    size_t row_ptr = 0, col_idx = 0, doc_count = 0, chunk_cnt = 0, total = 0;
+    size_t row_ptr = 0, col_idx = 0, doc_count = 0, chunk_cnt = 0, row_bounds = 0, rowidx = 0, total = 0;
 };
 
 BwdLayout backward_layout(int32_t n_q, int32_t lq_max, int32_t n_docs, int64_t total) {
@@ -143,7 +175,9 @@ BwdLayout backward_layout(int32_t n_q, int32_t lq_max, int32_t n_docs, int64_t t
     l.col_idx = align_up(static_cast<size_t>(std::max<int64_t>(1, int64_t(n_q) * n_docs * lq_max)) * 4);
     l.doc_count = align_up(static_cast<size_t>(n_docs + 1) * 4);
     l.chunk_cnt = align_up(static_cast<size_t>(csr_chunks(n_q, lq_max, n_docs)) * std::max<int64_t>(total, 1) * 4);
-    l.total = l.row_ptr + l.col_idx + l.doc_count + l.chunk_cnt;
+    l.row_bounds = align_up(static_cast<size_t>(sort_chunks(n_q, lq_max)) * std::max<int64_t>(total, 1) * 4);
+    l.rowidx = l.col_idx;   // dQ's per-row lists of D rows: one int32 per argmax entry
+    l.total = l.row_ptr + 2 * l.col_idx + l.doc_count + l.chunk_cnt + 2 * l.row_bounds + l.rowidx;
     return l;
 }
 
@@ -820,7 +854,13 @@ static void fill_bwd_params(BwdParams &p, const int32_t *argmax, const int32_t *
     p.col_idx = reinterpret_cast<int32_t *>(ws + l.row_ptr);
     p.doc_count = reinterpret_cast<int32_t *>(ws + l.row_ptr + l.col_idx);
     p.chunk_cnt = reinterpret_cast<int32_t *>(ws + l.row_ptr + l.col_idx + l.doc_count);
+    p.row_start = reinterpret_cast<int32_t *>(ws + l.row_ptr + l.col_idx + l.doc_count + l.chunk_cnt);
+    p.row_end = reinterpret_cast<int32_t *>(ws + l.row_ptr + l.col_idx + l.doc_count + l.chunk_cnt + l.row_bounds);
+    p.col_w = reinterpret_cast<float *>(ws + l.row_ptr + l.col_idx + l.doc_count + l.chunk_cnt + 2 * l.row_bounds);
     p.chunks = csr_chunks(n_q, lq_max, n_docs);
+    p.sort_chunks = sort_chunks(n_q, lq_max);
+    p.sort_chunk_len = static_cast<int32_t>(
+        std::max<int64_t>(1, (static_cast<int64_t>(n_q) * lq_max + p.sort_chunks - 1) / p.sort_chunks));
     make_divisor(std::max(1, lq_max), p.lq_magic, p.lq_shift);
     p.status = di.status;
 }
@@ -848,7 +888,7 @@ static maxsim_status_t backward_impl(const float *grad_scores, const int32_t *ar
                                      const int32_t *q_lens, int32_t n_q, int32_t lq_max, const void *D,
                                      const int32_t *cu_seqlens, int32_t n_docs, int64_t total_d_tokens,
                                      int32_t dim, maxsim_dtype_t dtype, float *dQ, float *dD, void *workspace,
-                                     size_t workspace_bytes, cudaStream_t stream, bool counts_ready) {
+                                     size_t workspace_bytes, cudaStream_t stream) {
     if (dtype == MAXSIM_INT8) return MAXSIM_ERR_UNSUPPORTED;
     if (dtype != MAXSIM_FP16 && dtype != MAXSIM_BF16) return MAXSIM_ERR_UNSUPPORTED;
     if (dim != kDim) return MAXSIM_ERR_UNSUPPORTED;
@@ -861,6 +901,8 @@ static maxsim_status_t backward_impl(const float *grad_scores, const int32_t *ar
         (total_d_tokens > 0 && (!aligned16(D) || !aligned16(dD))))
         return MAXSIM_ERR_INVALID_ARGUMENT;
     if (n_q > 0 && n_docs > 0 && !grad_scores) return MAXSIM_ERR_INVALID_ARGUMENT;
+    // a document's candidates must fit the backward's shared-memory sort
+    if (static_cast<int64_t>(n_q) * lq_max > kBackwardMaxCandidates) return MAXSIM_ERR_UNSUPPORTED;
     const BwdLayout l = backward_layout(n_q, lq_max, n_docs, total_d_tokens);
     if (!workspace || workspace_bytes < l.total) return MAXSIM_ERR_WORKSPACE;
     DeviceInfo di;
@@ -873,10 +915,21 @@ static maxsim_status_t backward_impl(const float *grad_scores, const int32_t *ar
     p.dQ = dQ;
     p.dD = dD;
     p.bf16 = dtype == MAXSIM_BF16;
-    cudaError_t e = launch_build_csr(p, stream, counts_ready);
-    if (e == cudaSuccess) e = launch_grad_d(p, stream);
-    if (e == cudaSuccess) e = launch_grad_q(p, stream);
-    return cuda_status(e);
+    int32_t *rowidx = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) + l.total - l.rowidx);
+    // dQ needs only the argmax: it runs on the device's side stream, forked
+    // from and joined back into `stream`, while dD's (latency-bound) sort and
+    // its reduction run here
+    std::lock_guard<std::mutex> lock(g_side_mu);
+    SideStream side;
+    if ((st = side_stream(&side)) != MAXSIM_OK) return st;
+    cudaError_t e = cudaEventRecord(side.fork, stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side.stream, side.fork, 0);
+    if (e == cudaSuccess) e = launch_grad_q(p, rowidx, side.stream);
+    if (e == cudaSuccess) e = cudaEventRecord(side.join, side.stream);
+    if (e != cudaSuccess) return MAXSIM_ERR_CUDA;
+    e = launch_sort_and_grad_d(p, stream);
+    const cudaError_t j = cudaStreamWaitEvent(stream, side.join, 0);   // joined even if a launch failed
+    return cuda_status(e != cudaSuccess ? e : j);
 }
 
 maxsim_status_t maxsim_backward(const float *grad_scores, const int32_t *argmax, const void *Q,
@@ -885,7 +938,7 @@ maxsim_status_t maxsim_backward(const float *grad_scores, const int32_t *argmax,
                                 int32_t dim, maxsim_dtype_t dtype, float *dQ, float *dD, void *workspace,
                                 size_t workspace_bytes, void *stream_) {
     return backward_impl(grad_scores, argmax, Q, q_lens, n_q, lq_max, D, cu_seqlens, n_docs, total_d_tokens, dim,
-                         dtype, dQ, dD, workspace, workspace_bytes, static_cast<cudaStream_t>(stream_), false);
+                         dtype, dQ, dD, workspace, workspace_bytes, static_cast<cudaStream_t>(stream_));
 }
 
 maxsim_status_t maxsim_forward_with_counts(const void *Q, const int32_t *q_lens, int32_t n_q, int32_t lq_max,
@@ -909,20 +962,11 @@ maxsim_status_t maxsim_forward_with_counts(const void *Q, const int32_t *q_lens,
     const BwdLayout bl = backward_layout(n_q, lq_max, n_docs, total_d_tokens);
     if (backward_workspace == nullptr || backward_workspace_bytes < bl.total) return MAXSIM_ERR_WORKSPACE;
 
-    uint8_t *bws = static_cast<uint8_t *>(backward_workspace);
-    int32_t *chunk_cnt = reinterpret_cast<int32_t *>(bws + bl.row_ptr + bl.col_idx + bl.doc_count);
-    // the counts start at zero; the per-document totals are summed from them
-    // by the backward
-    if (cudaMemsetAsync(chunk_cnt, 0, bl.chunk_cnt, stream) != cudaSuccess) return MAXSIM_ERR_CUDA;
     ForwardPlan plan;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     st = forward_prepare(plan, Q, q_lens, n_q, lq_max, dtype, 1.0f, 1.0f, ws, ws + wl.partials, stream);
     if (st != MAXSIM_OK) return st;
-    const int chunks = csr_chunks(n_q, lq_max, n_docs);
-    const int64_t n_cand = static_cast<int64_t>(n_q) * lq_max;
-    plan.p.csr_cnt = chunk_cnt;
-    plan.p.csr_chunks = chunks;
-    plan.p.csr_chunk_len = static_cast<int32_t>(std::max<int64_t>(1, (n_cand + chunks - 1) / chunks));
+    // the backward sorts each document's sources itself: nothing to count
     return forward_block(plan, D, cu_seqlens, n_docs, total_d_tokens, scores, nullptr, argmax, n_docs, stream);
 }
 
@@ -932,7 +976,7 @@ maxsim_status_t maxsim_backward_with_counts(const float *grad_scores, const int3
                                             int32_t dim, maxsim_dtype_t dtype, float *dQ, float *dD,
                                             void *workspace, size_t workspace_bytes, void *stream_) {
     return backward_impl(grad_scores, argmax, Q, q_lens, n_q, lq_max, D, cu_seqlens, n_docs, total_d_tokens, dim,
-                         dtype, dQ, dD, workspace, workspace_bytes, static_cast<cudaStream_t>(stream_), true);
+                         dtype, dQ, dD, workspace, workspace_bytes, static_cast<cudaStream_t>(stream_));
 }
 
 maxsim_status_t maxsim_forward_plan(int32_t n_q, int32_t lq_max, int32_t n_docs, int64_t total_d_tokens,
@@ -955,6 +999,18 @@ maxsim_status_t maxsim_forward_plan(int32_t n_q, int32_t lq_max, int32_t n_docs,
     layout[3] = static_cast<int32_t>(l.parts);
     layout[4] = l.ksplit ? 1 : 0;
     return MAXSIM_OK;
+}
+
+maxsim_status_t maxsim_probe_l2_read(const void *buf, size_t bytes, int32_t passes, uint64_t *sink,
+                                     void *stream_) {
+    if (!buf || !sink || bytes < 16 || bytes % 16 != 0 || !aligned16(buf) || passes <= 0)
+        return MAXSIM_ERR_INVALID_ARGUMENT;
+    DeviceInfo di;
+    maxsim_status_t st = device_info(&di);
+    if (st != MAXSIM_OK) return st;
+    const int ctas = std::min(kProbeSinkWords, 2 * di.sm_count);
+    return cuda_status(launch_l2_read_probe(buf, bytes, passes, reinterpret_cast<unsigned long long *>(sink), ctas,
+                                            static_cast<cudaStream_t>(stream_)));
 }
 
 maxsim_status_t maxsim_selftest_bounded_wait(uint32_t limit_us, void *stream_) {

@@ -185,3 +185,14 @@ def test_noalloc_binding_checks_outputs_before_any_call(lib):
     # the allocating forward checks caller-provided outputs the same way
     with pytest.raises(ValueError, match="scores must have shape"):
         m.maxsim_forward(Q, ql, D, cu, scores=torch.zeros((3, 2)))
+
+
+def test_l2_probe_rejects_bad_arguments(lib):
+    """Argument errors return before any device work."""
+    vp = ctypes.c_void_p
+    p = lib.maxsim_probe_l2_read
+    assert p(None, 1 << 20, 1, vp(256), None) == 1        # no buffer
+    assert p(vp(256), 1 << 20, 1, None, None) == 1        # no sink
+    assert p(vp(264), 1 << 20, 1, vp(256), None) == 1     # buffer off a 16-byte boundary
+    assert p(vp(256), 1000, 1, vp(256), None) == 1        # not a multiple of 16 bytes
+    assert p(vp(256), 1 << 20, 0, vp(256), None) == 1     # no pass

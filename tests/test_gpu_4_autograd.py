@@ -52,8 +52,8 @@ def test_autograd_matches_torch_reference(ops, dtype):
 
 @pytest.mark.parametrize("lq", [32, 100])
 def test_autograd_grads_equal_the_c_abi_backward(ops, lq):
-    """Bit-equal to the C ABI's forward + backward: with the counting pair
-    (32-token queries) and with the plain pair (100-token queries)."""
+    """Bit-equal to the C ABI's forward + backward (32- and 100-token
+    queries)."""
     from late_interaction_retrieval_maxsim_gb300.autograd import maxsim
     Q, ql, D, cu = random_case(4, lq, [180] * 16, "bf16", seed=78)
     Qa = Q.clone().requires_grad_(True)
@@ -68,9 +68,8 @@ def test_autograd_grads_equal_the_c_abi_backward(ops, lq):
 
 
 def test_autograd_second_backward_through_the_same_graph(ops):
-    """The first backward uses (and consumes) the forward's CSR counts; a
-    second one through the retained graph counts from the argmax and must
-    give the same gradients."""
+    """A second backward through the retained graph gives the same
+    gradients as the first."""
     from late_interaction_retrieval_maxsim_gb300.autograd import maxsim
     Q, ql, D, cu = random_case(4, 32, [180] * 8, "bf16", seed=79)
     Qa = Q.clone().requires_grad_(True)

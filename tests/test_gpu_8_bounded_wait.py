@@ -42,3 +42,23 @@ def test_limit_out_of_range_is_rejected(ops):
     with pytest.raises(Exception):
         ops.maxsim_selftest_bounded_wait(2_000_000)
     assert ops.maxsim_device_status() == 0
+
+
+def test_l2_read_probe_reads_every_word(ops):
+    """The L2 read probe (the measuring stick of the backward's roofline)
+    folds every 16-byte word it reads into its sink: with one pass the XOR of
+    all sink words equals the XOR of all 32-bit words of the buffer."""
+    import numpy as np
+    g = torch.Generator("cuda").manual_seed(5)
+    buf = torch.randint(-2**31, 2**31 - 1, (3 << 20,), generator=g, dtype=torch.int64, device="cuda")
+    buf = buf.to(torch.int32)                       # 12 MiB of random words
+    sink = ops.maxsim_probe_l2_read(buf, 1)
+    torch.cuda.synchronize()
+    words = buf.cpu().numpy().view(np.uint32)
+    want = int(np.bitwise_xor.reduce(words))
+    got = int(np.bitwise_xor.reduce(sink.cpu().numpy().view(np.uint64)))
+    assert got == want
+    # an even number of passes cancels out
+    sink2 = ops.maxsim_probe_l2_read(buf, 2)
+    torch.cuda.synchronize()
+    assert int(np.bitwise_xor.reduce(sink2.cpu().numpy().view(np.uint64))) == 0
