@@ -390,9 +390,18 @@ def _int8_variants(m, syn, steps=10):
                                   max_doc_len=w.ld_hi, workspace=ws)
     _, per = _time_loop(rerank, steps, 3, stream)
     ms = statistics.median(per)
+    # what the scan competes with: exact FP16 scoring of every document, and
+    # its stage 1 alone (the INT8 scan of every document, value only)
+    s16 = torch.empty((w.n_q, w.n_docs), dtype=torch.float32, device=dev)
+    _, per16 = _time_loop(lambda: m.maxsim_forward(Q16, ql, D16, cu, with_argmax=False, scores=s16), steps, 3, stream)
+    _, per8 = _time_loop(lambda: m.maxsim_forward(Q8, ql, D8, cu, with_argmax=False, scores=s16, q_scale=qst,
+                                                  d_scale=dst), steps, 3, stream)
     out["rerank_two_stage"] = {"n_q": w.n_q, "lq": w.lq, "n_docs": w.n_docs, "k_candidates": kc, "k": k,
                                "stage1": "int8 per tensor", "stage2": "fp16, corpus in HBM",
-                               "call_ms": round(ms, 4), "queries_per_s": w.n_q / (ms / 1e3)}
+                               "call_ms": round(ms, 4), "queries_per_s": w.n_q / (ms / 1e3),
+                               "fp16_exact_all_docs_value_only_ms": round(statistics.median(per16), 4),
+                               "int8_scan_all_docs_value_only_ms": round(statistics.median(per8), 4)}
+    del s16
     if m.maxsim_device_status() != 0:
         out["device_status"] = "fault"
     del Q8, D8, Q16, D16, ws

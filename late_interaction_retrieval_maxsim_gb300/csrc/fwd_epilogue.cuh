@@ -317,10 +317,15 @@ __device__ __forceinline__ void epilogue_warp(const FwdParams &p, int rho_warp, 
             for (int k4 = 0; k4 < 4; ++k4) {
                 const float4 v = reinterpret_cast<const float4 *>(scale_slot)[k4];
                 const int k = 16 * h + 4 * k4;
-                r[k] = __float_as_uint(__uint_as_float(r[k]) * v.x);
-                r[k + 1] = __float_as_uint(__uint_as_float(r[k + 1]) * v.y);
-                r[k + 2] = __float_as_uint(__uint_as_float(r[k + 2]) * v.z);
-                r[k + 3] = __float_as_uint(__uint_as_float(r[k + 3]) * v.w);
+                // two IEEE products per instruction (the same roundings as scalar ones)
+                const float2 lo = mul2(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])),
+                                       make_float2(v.x, v.y));
+                const float2 hi = mul2(make_float2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3])),
+                                       make_float2(v.z, v.w));
+                r[k] = __float_as_uint(lo.x);
+                r[k + 1] = __float_as_uint(lo.y);
+                r[k + 2] = __float_as_uint(hi.x);
+                r[k + 3] = __float_as_uint(hi.y);
             }
         }
     };
@@ -425,6 +430,11 @@ __device__ __forceinline__ void epilogue_warp(const FwdParams &p, int rho_warp, 
 
     uint32_t ra[32];
     [[maybe_unused]] uint32_t rb[32];
+    [[maybe_unused]] float sc_cur[4] = {0.f, 0.f, 0.f, 0.f}, sc_nxt[4] = {0.f, 0.f, 0.f, 0.f};
+    if constexpr (SCALE && !DB)
+        if (warp_rows)
+#pragma unroll
+            for (int kc = 0; kc < 4; ++kc) sc_nxt[kc] = chunk_scale(t_begin + 32 * kc);
     for (int j = 0; j < n_tiles; ++j) {
         const int2 su = slot_of(j);
         const int slot = su.x;
@@ -474,10 +484,20 @@ __device__ __forceinline__ void epilogue_warp(const FwdParams &p, int rho_warp, 
                 }
             }
         } else {
+            // SCALE: this tile's column scales were loaded one tile ahead (lane
+            // l holds column 32 kc + l of chunk kc); load the next tile's now
+            if constexpr (SCALE) {
+#pragma unroll
+                for (int kc = 0; kc < 4; ++kc) {
+                    sc_cur[kc] = sc_nxt[kc];
+                    sc_nxt[kc] = chunk_scale(tile0 + kBlockN + 32 * kc);
+                }
+            }
             // registers are scarce with 18-20 warps per SM: one chunk at a time
 #pragma unroll 1
             for (int kc = 0; kc < 4; ++kc) {
-                [[maybe_unused]] const float sc = chunk_scale(tile0 + 32 * kc);
+                [[maybe_unused]] float sc = 0.0f;
+                if constexpr (SCALE) sc = kc == 0 ? sc_cur[0] : kc == 1 ? sc_cur[1] : kc == 2 ? sc_cur[2] : sc_cur[3];
                 __syncwarp();
                 tmem_ld32_async(tb + 32 * kc, ra);
                 tmem_wait_ld(ra);

@@ -265,6 +265,21 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
     return r;
 }
 
+// Two FP32 lanes at once: d = a * b elementwise on (x, y) pairs (each an IEEE
+// product, rounded to nearest even).
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    uint64_t d;
+    asm("{\n\t.reg .b64 ra, rb;\n\t"
+        "mov.b64 ra, {%1, %2};\n\t"
+        "mov.b64 rb, {%3, %4};\n\t"
+        "mul.rn.f32x2 %0, ra, rb;\n\t}"
+        : "=l"(d)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
+    return r;
+}
+
 // 3-input maximum (sm_100 family).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
