@@ -374,35 +374,58 @@ __device__ __forceinline__ void warp_store_row(float *out_row, float2 (&acc)[4])
 // into C <= 32 chunks; one CTA per (document, chunk) keeps its chunk's
 // tokens in shared memory and sorts the chunk's sources by token with a
 // stable counting sort (per-warp histograms, a prefix over (token, warp),
-// ranks within a warp from __match_any_sync), kSortWin tokens at a time.  It
-// writes the sorted candidates k (the source's Q row) to the fixed slots
-// [b * n_cand + k0, b * n_cand + k1) of `list`, and for every token r of the
-// document the bounds of its run there to row_start / row_end[r * C + c],
-// and each source's g[q, b] to the same slot of col_w.  No prefix over
-// documents is needed, and token r's runs read chunk after chunk give its sources in
-// ascending order: the CSR's row.
-constexpr int kSortWarps = 8;
-constexpr int kSortThreads = 32 * kSortWarps;
+// ranks within a warp from ballots), WIN tokens at a time.  It writes the
+// sorted candidates k (the source's Q row) to the fixed slots
+// [b * n_cand + k0, b * n_cand + k1) of col_idx, each source's g[q, b] to the
+// same slot of col_w, and for every token r of the document the bounds of
+// its run there to row_start / row_end[r * C + c].  No prefix over documents
+// is needed, and token r's runs read chunk after chunk give its sources in
+// ascending order: the CSR's row.  (Measured alternatives: a two-pass LSD
+// radix sort on 5-bit digits was slower, 38.5 vs 23.5 us on the training
+// shape.)
 constexpr int kSortQueries = 1024;   // queries of a chunk whose q_lens and g are staged
 
+// The lanes of the warp whose (key, valid) equals this lane's, for keys below
+// 2^BITS: one ballot per key bit and one for validity (what
+// __match_any_sync returns; measured far cheaper than that instruction on 32
+// mostly distinct keys: the training-shape sort 29 -> 23.5 us).
+template <int BITS>
+__device__ __forceinline__ unsigned match_lanes(int key, bool valid) {
+    unsigned eq = __ballot_sync(0xffffffffu, valid);
+    if (!valid) eq = ~eq;
+#pragma unroll
+    for (int bit = 0; bit < BITS; ++bit) {
+        const bool on = (key >> bit) & 1;
+        const unsigned m = __ballot_sync(0xffffffffu, on);
+        eq &= on ? m : ~m;
+    }
+    return eq;
+}
+
 // WIN tokens per window: 256 for documents of a few hundred tokens, 1024 for
-// page-length ones (each window rescans the chunk's tokens in shared memory).
-template <int WIN>
+// page-length ones (each window rescans the chunk's tokens in shared memory);
+// W warps, each owning a contiguous segment of the chunk.  Short documents
+// use 16 warps; the 1024-token histograms leave room for 8.
+template <int WIN, int W>
 size_t sort_smem_bytes(int chunk_len) {
     // tokens, per-warp histograms, run starts, and the window's sorted output
     // (candidate and weight) staged for coalesced writes
-    return static_cast<size_t>(chunk_len) * 4 * 3 + kSortWarps * WIN * 4 + (WIN + 1) * 4 + 16;
+    return static_cast<size_t>(chunk_len) * 4 * 3 + W * WIN * 4 + (WIN + 1) * 4 + 16;
 }
 
-template <int WIN>
-__global__ void __launch_bounds__(kSortThreads) bwd_sort_kernel(BwdParams p) {
+template <int WIN, int W>
+__global__ void __launch_bounds__(32 * W) bwd_sort_kernel(BwdParams p) {
+    constexpr int T = 32 * W;
+    constexpr int PER = WIN >= T ? WIN / T : 1;   // tokens per thread in the scan
+    constexpr int KB = WIN == 256 ? 8 : 10;       // token bits
+    static_assert((1 << KB) == WIN, "window tokens fit the key bits");
     extern __shared__ __align__(16) uint8_t ssm[];
     int32_t *tok = reinterpret_cast<int32_t *>(ssm);                 // [chunk_len]
     int32_t *hist = tok + p.sort_chunk_len;                          // [W][WIN]
-    int32_t *start = hist + kSortWarps * WIN;                        // [WIN + 1]
+    int32_t *start = hist + W * WIN;                                 // [WIN + 1]
     int32_t *out_k = start + WIN + 1;                                // [chunk_len] the window's sorted sources
     float *out_w = reinterpret_cast<float *>(out_k + p.sort_chunk_len);   // [chunk_len] their weights
-    __shared__ int32_t warp_tot[kSortWarps];
+    __shared__ int32_t warp_tot[W];
     __shared__ int32_t s_ql[kSortQueries];
     __shared__ float s_g[kSortQueries];
     const int C = p.sort_chunks;
@@ -421,23 +444,26 @@ __global__ void __launch_bounds__(kSortThreads) bwd_sort_kernel(BwdParams p) {
     const int n_qr = len > 0 ? query_of(p, k0 + len - 1) - q_lo + 1 : 0;
     const bool staged = n_qr <= kSortQueries;
     if (staged)
-        for (int qq = threadIdx.x; qq < n_qr; qq += kSortThreads) {
+        for (int qq = threadIdx.x; qq < n_qr; qq += T) {
             s_ql[qq] = p.q_lens[q_lo + qq];
             s_g[qq] = p.grad[static_cast<int64_t>(q_lo + qq) * p.n_docs + b];
         }
+    for (int k = threadIdx.x; k < W * WIN; k += T) hist[k] = 0;
     __syncthreads();
     auto qlen_of = [&](int q) { return staged ? s_ql[q - q_lo] : p.q_lens[q]; };
     auto g_of = [&](int q) { return staged ? s_g[q - q_lo] : p.grad[static_cast<int64_t>(q) * p.n_docs + b]; };
 
-    // 1. the chunk's candidates: the token each names, or -1 (four loads in
-    //    flight per thread)
-    for (int kb = threadIdx.x; kb < len; kb += 4 * kSortThreads) {
+    const int seg = ((len + W - 1) / W + 31) / 32 * 32;
+    const int s_lo = min(len, warp * seg), s_hi = min(len, s_lo + seg);
+    // 1. the warp's segment: the token each candidate names, or -1 (four loads
+    //    in flight per lane), counted at once for the first window
+    for (int kb = s_lo + lane; kb < s_hi; kb += 4 * 32) {
         int a[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const int kk = kb + u * kSortThreads;
+            const int kk = kb + 32 * u;
             a[u] = -1;
-            if (kk < len) {
+            if (kk < s_hi) {
                 const int k = k0 + kk;
                 const int q = query_of(p, k);
                 const int i = k - q * p.lq_max;
@@ -446,39 +472,42 @@ __global__ void __launch_bounds__(kSortThreads) bwd_sort_kernel(BwdParams p) {
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const int kk = kb + u * kSortThreads;
-            if (kk >= len) continue;
+            const int kk = kb + 32 * u;
+            if (kk >= s_hi) continue;
             int v = a[u];
             if (v < -1 || v >= ld) {
                 atomicCAS(p.status, 0, ptx::kStatusBadArgmax);
                 v = -1;
             }
             tok[kk] = v;
+            if (v >= 0 && v < WIN) atomicAdd(&hist[warp * WIN + v], 1);
         }
     }
-    const int seg = ((len + kSortWarps - 1) / kSortWarps + 31) / 32 * 32;
-    const int s_lo = min(len, warp * seg), s_hi = min(len, s_lo + seg);
     int32_t win_base = b * n_cand + k0;   // first slot of the current window's sources (< 2^31)
 
     for (int w0 = 0; w0 < ld; w0 += WIN) {
         const int win = min(WIN, ld - w0);
-        for (int k = threadIdx.x; k < kSortWarps * WIN; k += kSortThreads) hist[k] = 0;
-        __syncthreads();
-        // 2. per-warp histograms of the window's tokens
-        for (int kk = s_lo + lane; kk < s_hi; kk += 32) {
-            const int t = tok[kk] - w0;
-            if (t >= 0 && t < win) atomicAdd(&hist[warp * WIN + t], 1);
+        if (w0 > 0) {
+            for (int k = threadIdx.x; k < W * WIN; k += T) hist[k] = 0;
+            __syncthreads();
+            // 2. per-warp histograms of the window's tokens
+            for (int kk = s_lo + lane; kk < s_hi; kk += 32) {
+                const int t = tok[kk] - w0;
+                if (t >= 0 && t < win) atomicAdd(&hist[warp * WIN + t], 1);
+            }
         }
         __syncthreads();
         // 3. token totals -> exclusive scan -> each warp's first slot per
         //    token (thread t holds tokens PER * t .. PER * t + PER - 1)
-        constexpr int PER = WIN / kSortThreads;
         const int t = threadIdx.x;
         int tot = 0;
 #pragma unroll
-        for (int e = 0; e < PER; ++e)
+        for (int e = 0; e < PER; ++e) {
+            const int tk = PER * t + e;
+            if (tk < WIN)
 #pragma unroll
-            for (int w = 0; w < kSortWarps; ++w) tot += hist[w * WIN + PER * t + e];
+                for (int w = 0; w < W; ++w) tot += hist[w * WIN + tk];
+        }
         int x = tot;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -492,17 +521,18 @@ __global__ void __launch_bounds__(kSortThreads) bwd_sort_kernel(BwdParams p) {
 #pragma unroll
         for (int e = 0; e < PER; ++e) {
             const int tk = PER * t + e;
+            if (tk >= WIN) break;
             start[tk] = run;
 #pragma unroll
-            for (int w = 0; w < kSortWarps; ++w) {
+            for (int w = 0; w < W; ++w) {
                 const int v = hist[w * WIN + tk];
                 hist[w * WIN + tk] = run;
                 run += v;
             }
         }
-        if (t == kSortThreads - 1) start[WIN] = run;
+        if (t == T - 1) start[WIN] = run;   // the last thread's tokens end the window
         __syncthreads();
-        for (int tk = t; tk < win; tk += kSortThreads) {
+        for (int tk = t; tk < win; tk += T) {
             rs[static_cast<int64_t>(w0 + tk) * C] = win_base + start[tk];
             re[static_cast<int64_t>(w0 + tk) * C] = win_base + start[tk + 1];
         }
@@ -511,8 +541,7 @@ __global__ void __launch_bounds__(kSortThreads) bwd_sort_kernel(BwdParams p) {
             const int kk = kb + lane;
             const int tt = kk < s_hi ? tok[kk] - w0 : -1;
             const bool mine = tt >= 0 && tt < win;
-            const int key = mine ? tt : (0x40000000 | lane);   // lanes without a source never match
-            const unsigned peers = __match_any_sync(0xffffffffu, key);
+            const unsigned peers = match_lanes<KB>(mine ? tt : 0, mine);
             const int rank = __popc(peers & ((1u << lane) - 1u));
             int pos = 0;
             if (mine) pos = hist[warp * WIN + tt] + rank;
@@ -527,7 +556,7 @@ __global__ void __launch_bounds__(kSortThreads) bwd_sort_kernel(BwdParams p) {
         __syncthreads();
         // 5. the window's sorted sources to their slots, coalesced
         const int n_win = start[WIN];
-        for (int e = threadIdx.x; e < n_win; e += kSortThreads) {
+        for (int e = threadIdx.x; e < n_win; e += T) {
             p.col_idx[win_base + e] = out_k[e];
             p.col_w[win_base + e] = out_w[e];
         }
@@ -711,16 +740,18 @@ int sort_chunks(int32_t n_q, int32_t lq_max) {
     return static_cast<int>(c < 1 ? 1 : (c > kSortMaxChunks ? kSortMaxChunks : c));
 }
 
-static_assert(kSortMaxChunkLen * 12 + kSortWarps * 1024 * 4 + 1025 * 4 + 16 + 2 * 4096 + 64 <= 227 * 1024,
-              "the largest sort chunk fits one CTA's shared memory");
+static_assert(kSortMaxChunkLen * 12 + 8 * 1024 * 4 + 1025 * 4 + 16 + 2 * 4096 + 64 <= 227 * 1024,
+              "the largest sort chunk fits one CTA's shared memory (1024-token windows, 8 warps)");
+static_assert(kSortMaxChunkLen * 12 + 16 * 256 * 4 + 257 * 4 + 16 + 2 * 4096 + 64 <= 227 * 1024,
+              "the largest sort chunk fits one CTA's shared memory (256-token windows, 16 warps)");
 
-template <int WIN>
+template <int WIN, int W>
 cudaError_t launch_sort(const BwdParams &p, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(bwd_sort_kernel<WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(sort_smem_bytes<WIN>(kSortMaxChunkLen)));
+    cudaError_t e = cudaFuncSetAttribute(bwd_sort_kernel<WIN, W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(sort_smem_bytes<WIN, W>(kSortMaxChunkLen)));
     if (e != cudaSuccess) return e;
-    bwd_sort_kernel<WIN><<<static_cast<unsigned>(p.n_docs) * p.sort_chunks, kSortThreads,
-                           sort_smem_bytes<WIN>(p.sort_chunk_len), stream>>>(p);
+    bwd_sort_kernel<WIN, W><<<static_cast<unsigned>(p.n_docs) * p.sort_chunks, 32 * W,
+                              sort_smem_bytes<WIN, W>(p.sort_chunk_len), stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -730,7 +761,7 @@ cudaError_t launch_sort_and_grad_d(const BwdParams &p, cudaStream_t stream) {
         return cudaMemsetAsync(p.dD, 0, sizeof(float) * 128 * static_cast<size_t>(p.total_tokens), stream);
     // windows of 1024 tokens when documents average more than 256
     const bool long_docs = p.total_tokens > 256 * static_cast<int64_t>(p.n_docs);
-    cudaError_t e = long_docs ? launch_sort<1024>(p, stream) : launch_sort<256>(p, stream);
+    cudaError_t e = long_docs ? launch_sort<1024, 8>(p, stream) : launch_sort<256, 16>(p, stream);
     if (e != cudaSuccess) return e;
     const int64_t threads = static_cast<int64_t>(p.total_tokens) * 32;
     grad_d_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(p);
