@@ -378,12 +378,23 @@ __device__ __forceinline__ void warp_store_row(float *out_row, float2 (&acc)[4])
 // sorted candidates k (the source's Q row) to the fixed slots
 // [b * n_cand + k0, b * n_cand + k1) of col_idx, each source's g[q, b] to the
 // same slot of col_w, and for every token r of the document the bounds of
-// its run there to row_start / row_end[r * C + c].  No prefix over documents
+// its run there to row_start / row_end at run_bound_index(r, c, C).  No prefix over documents
 // is needed, and token r's runs read chunk after chunk give its sources in
 // ascending order: the CSR's row.  (Measured alternatives: a two-pass LSD
 // radix sort on 5-bit digits was slower, 38.5 vs 23.5 us on the training
 // shape.)
-constexpr int kSortQueries = 1024;   // queries of a chunk whose q_lens and g are staged
+constexpr int kSortQueries = 256;   // queries of a chunk whose q_lens and g are staged
+
+// Per-warp histograms are stored with one pad word after every 32 tokens, so
+// the scan's threads (each reading PER consecutive tokens) hit distinct banks.
+// (Two tokens per word as 16-bit halves, which halves this array, measured
+// 264 -> 260 us for the ColPali-shape backward but 145 -> 149 us for the
+// training shape, and is not used.)
+template <int WIN>
+struct SortHist {
+    static constexpr int kStride = WIN + WIN / 32;   // words per warp
+    __device__ static __forceinline__ int at(int t) { return t + (t >> 5); }
+};
 
 // The lanes of the warp whose (key, valid) equals this lane's, for keys below
 // 2^BITS: one ballot per key bit and one for validity (what
@@ -410,7 +421,7 @@ template <int WIN, int W>
 size_t sort_smem_bytes(int chunk_len) {
     // tokens, per-warp histograms, run starts, and the window's sorted output
     // (candidate and weight) staged for coalesced writes
-    return static_cast<size_t>(chunk_len) * 4 * 3 + W * WIN * 4 + (WIN + 1) * 4 + 16;
+    return static_cast<size_t>(chunk_len) * 4 * 3 + W * SortHist<WIN>::kStride * 4 + (WIN + 1) * 4 + 16;
 }
 
 template <int WIN, int W>
@@ -419,10 +430,12 @@ __global__ void __launch_bounds__(32 * W) bwd_sort_kernel(BwdParams p) {
     constexpr int PER = WIN >= T ? WIN / T : 1;   // tokens per thread in the scan
     constexpr int KB = WIN == 256 ? 8 : 10;       // token bits
     static_assert((1 << KB) == WIN, "window tokens fit the key bits");
+    using H = SortHist<WIN>;
+    constexpr int HS = H::kStride;
     extern __shared__ __align__(16) uint8_t ssm[];
     int32_t *tok = reinterpret_cast<int32_t *>(ssm);                 // [chunk_len]
-    int32_t *hist = tok + p.sort_chunk_len;                          // [W][WIN]
-    int32_t *start = hist + W * WIN;                                 // [WIN + 1]
+    int32_t *hist = tok + p.sort_chunk_len;                          // [W][HS], token t at H::at(t)
+    int32_t *start = hist + W * HS;                                  // [WIN + 1]
     int32_t *out_k = start + WIN + 1;                                // [chunk_len] the window's sorted sources
     float *out_w = reinterpret_cast<float *>(out_k + p.sort_chunk_len);   // [chunk_len] their weights
     __shared__ int32_t warp_tot[W];
@@ -437,8 +450,7 @@ __global__ void __launch_bounds__(32 * W) bwd_sort_kernel(BwdParams p) {
     const int n_cand = p.n_q * p.lq_max;
     const int k0 = min(n_cand, c * p.sort_chunk_len);
     const int len = min(n_cand, k0 + p.sort_chunk_len) - k0;
-    int32_t *rs = p.row_start + static_cast<int64_t>(t0) * C + c;
-    int32_t *re = p.row_end + static_cast<int64_t>(t0) * C + c;
+
     // q_lens and g[., b] of the chunk's queries, when they are few enough
     const int q_lo = len > 0 ? query_of(p, k0) : 0;
     const int n_qr = len > 0 ? query_of(p, k0 + len - 1) - q_lo + 1 : 0;
@@ -448,7 +460,7 @@ __global__ void __launch_bounds__(32 * W) bwd_sort_kernel(BwdParams p) {
             s_ql[qq] = p.q_lens[q_lo + qq];
             s_g[qq] = p.grad[static_cast<int64_t>(q_lo + qq) * p.n_docs + b];
         }
-    for (int k = threadIdx.x; k < W * WIN; k += T) hist[k] = 0;
+    for (int k = threadIdx.x; k < W * HS; k += T) hist[k] = 0;
     __syncthreads();
     auto qlen_of = [&](int q) { return staged ? s_ql[q - q_lo] : p.q_lens[q]; };
     auto g_of = [&](int q) { return staged ? s_g[q - q_lo] : p.grad[static_cast<int64_t>(q) * p.n_docs + b]; };
@@ -480,7 +492,7 @@ __global__ void __launch_bounds__(32 * W) bwd_sort_kernel(BwdParams p) {
                 v = -1;
             }
             tok[kk] = v;
-            if (v >= 0 && v < WIN) atomicAdd(&hist[warp * WIN + v], 1);
+            if (v >= 0 && v < WIN) atomicAdd(&hist[warp * HS + H::at(v)], 1);
         }
     }
     int32_t win_base = b * n_cand + k0;   // first slot of the current window's sources (< 2^31)
@@ -488,12 +500,12 @@ __global__ void __launch_bounds__(32 * W) bwd_sort_kernel(BwdParams p) {
     for (int w0 = 0; w0 < ld; w0 += WIN) {
         const int win = min(WIN, ld - w0);
         if (w0 > 0) {
-            for (int k = threadIdx.x; k < W * WIN; k += T) hist[k] = 0;
+            for (int k = threadIdx.x; k < W * HS; k += T) hist[k] = 0;
             __syncthreads();
             // 2. per-warp histograms of the window's tokens
             for (int kk = s_lo + lane; kk < s_hi; kk += 32) {
                 const int t = tok[kk] - w0;
-                if (t >= 0 && t < win) atomicAdd(&hist[warp * WIN + t], 1);
+                if (t >= 0 && t < win) atomicAdd(&hist[warp * HS + H::at(t)], 1);
             }
         }
         __syncthreads();
@@ -506,7 +518,7 @@ __global__ void __launch_bounds__(32 * W) bwd_sort_kernel(BwdParams p) {
             const int tk = PER * t + e;
             if (tk < WIN)
 #pragma unroll
-                for (int w = 0; w < W; ++w) tot += hist[w * WIN + tk];
+                for (int w = 0; w < W; ++w) tot += hist[w * HS + H::at(tk)];
         }
         int x = tot;
 #pragma unroll
@@ -525,16 +537,17 @@ __global__ void __launch_bounds__(32 * W) bwd_sort_kernel(BwdParams p) {
             start[tk] = run;
 #pragma unroll
             for (int w = 0; w < W; ++w) {
-                const int v = hist[w * WIN + tk];
-                hist[w * WIN + tk] = run;
+                const int v = hist[w * HS + H::at(tk)];
+                hist[w * HS + H::at(tk)] = run;
                 run += v;
             }
         }
         if (t == T - 1) start[WIN] = run;   // the last thread's tokens end the window
         __syncthreads();
         for (int tk = t; tk < win; tk += T) {
-            rs[static_cast<int64_t>(w0 + tk) * C] = win_base + start[tk];
-            re[static_cast<int64_t>(w0 + tk) * C] = win_base + start[tk + 1];
+            const int64_t at = run_bound_index(t0 + w0 + tk, c, C);
+            p.row_start[at] = win_base + start[tk];
+            p.row_end[at] = win_base + start[tk + 1];
         }
         // 4. stable placement, 32 candidates at a time per warp
         for (int kb = s_lo; kb < s_hi; kb += 32) {
@@ -544,12 +557,12 @@ __global__ void __launch_bounds__(32 * W) bwd_sort_kernel(BwdParams p) {
             const unsigned peers = match_lanes<KB>(mine ? tt : 0, mine);
             const int rank = __popc(peers & ((1u << lane) - 1u));
             int pos = 0;
-            if (mine) pos = hist[warp * WIN + tt] + rank;
+            if (mine) pos = hist[warp * HS + H::at(tt)] + rank;
             __syncwarp();
             if (mine) {
                 out_k[pos] = k0 + kk;
                 out_w[pos] = g_of(query_of(p, k0 + kk));
-                if (rank == 0) hist[warp * WIN + tt] += __popc(peers);
+                if (rank == 0) hist[warp * HS + H::at(tt)] += __popc(peers);
             }
             __syncwarp();
         }
@@ -579,16 +592,31 @@ __device__ __forceinline__ int rotation(int64_t row, int n) {
 // (ascending source order, the CSR's row) as one list of n entries: lane c <
 // C holds run c's bounds, and a position maps to its run by a prefix over the
 // run lengths.  The sum visits the list from position rotation(r, n),
-// wrapping around.
-__global__ void __launch_bounds__(256) grad_d_kernel(BwdParams p) {
-    const int r = static_cast<int>((blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5);
+// wrapping around.  A CTA's kRunBlock rows read their bounds as one
+// contiguous range, staged through shared memory.
+__global__ void __launch_bounds__(32 * kRunBlock) grad_d_kernel(BwdParams p) {
+    constexpr int kPitch = 36;   // words per row: 36 j + c spreads a 32-thread store over all banks
+    static_assert(kSortMaxChunks <= kPitch, "a row's bounds fit its pitch");
+    __shared__ int32_t s_lo[kRunBlock * kPitch], s_hi[kRunBlock * kPitch];
+    const int C = p.sort_chunks;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kRunBlock;
+    const int64_t base = r0 * C;   // run_bound_index(r0, 0, C)
+    for (int e = threadIdx.x; e < C * kRunBlock; e += blockDim.x) {
+        const int c = e / kRunBlock, j = e - c * kRunBlock;
+        if (r0 + j < p.total_tokens) {
+            s_lo[j * kPitch + c] = __ldg(p.row_start + base + e);
+            s_hi[j * kPitch + c] = __ldg(p.row_end + base + e);
+        }
+    }
+    __syncthreads();
+    const int r = static_cast<int>(r0) + (threadIdx.x >> 5);
     if (r >= p.total_tokens) return;
     const int lane = threadIdx.x & 31;
-    const int C = p.sort_chunks;
+    const int wr = threadIdx.x >> 5;   // this warp's row within the block
     int lo = 0, len = 0;
     if (lane < C) {
-        lo = p.row_start[static_cast<int64_t>(r) * C + lane];
-        len = p.row_end[static_cast<int64_t>(r) * C + lane] - lo;
+        lo = s_lo[wr * kPitch + lane];
+        len = s_hi[wr * kPitch + lane] - lo;
     }
     int incl = len;   // inclusive prefix of the run lengths over lanes
 #pragma unroll
@@ -734,15 +762,19 @@ cudaError_t launch_build_csr(const BwdParams &p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// (Chunks of 4096 for page-length documents halve the scan work per
+// candidate but fit fewer CTAs per SM: the ColPali-shape sort went 52 -> 57 us.)
 int sort_chunks(int32_t n_q, int32_t lq_max) {
     const int64_t n_cand = static_cast<int64_t>(n_q) * lq_max;
     const int64_t c = (n_cand + kSortChunkTarget - 1) / kSortChunkTarget;
     return static_cast<int>(c < 1 ? 1 : (c > kSortMaxChunks ? kSortMaxChunks : c));
 }
 
-static_assert(kSortMaxChunkLen * 12 + 8 * 1024 * 4 + 1025 * 4 + 16 + 2 * 4096 + 64 <= 227 * 1024,
+static_assert(kSortMaxChunkLen * 12 + 8 * SortHist<1024>::kStride * 4 + 1025 * 4 + 16 + 8 * kSortQueries + 64 <=
+                  227 * 1024,
               "the largest sort chunk fits one CTA's shared memory (1024-token windows, 8 warps)");
-static_assert(kSortMaxChunkLen * 12 + 16 * 256 * 4 + 257 * 4 + 16 + 2 * 4096 + 64 <= 227 * 1024,
+static_assert(kSortMaxChunkLen * 12 + 16 * SortHist<256>::kStride * 4 + 257 * 4 + 16 + 8 * kSortQueries + 64 <=
+                  227 * 1024,
               "the largest sort chunk fits one CTA's shared memory (256-token windows, 16 warps)");
 
 template <int WIN, int W>
@@ -760,11 +792,11 @@ cudaError_t launch_sort_and_grad_d(const BwdParams &p, cudaStream_t stream) {
     if (static_cast<int64_t>(p.n_q) * p.lq_max == 0)   // no source: every row is 0
         return cudaMemsetAsync(p.dD, 0, sizeof(float) * 128 * static_cast<size_t>(p.total_tokens), stream);
     // windows of 1024 tokens when documents average more than 256
-    const bool long_docs = p.total_tokens > 256 * static_cast<int64_t>(p.n_docs);
+    const bool long_docs = sort_long_docs(p.total_tokens, p.n_docs);
     cudaError_t e = long_docs ? launch_sort<1024, 8>(p, stream) : launch_sort<256, 16>(p, stream);
     if (e != cudaSuccess) return e;
-    const int64_t threads = static_cast<int64_t>(p.total_tokens) * 32;
-    grad_d_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(p);
+    const int64_t blocks = (static_cast<int64_t>(p.total_tokens) + kRunBlock - 1) / kRunBlock;
+    grad_d_kernel<<<static_cast<unsigned>(blocks), 32 * kRunBlock, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -117,8 +117,8 @@ struct BwdParams {
     int32_t *col_idx;        // [n_q * n_docs * lq_max]
     int32_t *doc_count;      // [n_docs + 1] scratch: sources per document, then offsets
     int32_t *chunk_cnt;      // [chunks * total] scratch: per-chunk token counts, then first slots
-    int32_t *row_start;      // [total * sort_chunks]: first col_idx slot of (token, chunk)'s sources
-    int32_t *row_end;        // [total * sort_chunks]: one past the last
+    int32_t *row_start;      // first col_idx slot of (chunk, token)'s sources, at run_bound_index
+    int32_t *row_end;        // one past the last
     float *col_w;            // [n_docs * n_q * lq_max]: the backward's sorted sources' g[q, b]
     int32_t sort_chunks, sort_chunk_len;   // candidate chunks per document of the backward's sort
     int32_t *status;
@@ -150,12 +150,25 @@ cudaError_t launch_grad_q(const BwdParams &p, int32_t *rowidx, cudaStream_t stre
 // in C = sort_chunks() chunks (about kSortChunkTarget each, at most
 // kSortMaxChunks chunks of at most kSortMaxChunkLen), sorted per (document,
 // chunk) in shared memory into fixed slots of col_idx (their g[q, b] in the
-// same slots of col_w), with per-(token, chunk) run bounds in row_start /
-// row_end; then one warp per dD row.
+// same slots of col_w), with per-(chunk, token) run bounds in row_start /
+// row_end; then one warp per dD row, kRunBlock rows per CTA.
 constexpr int kSortChunkTarget = 2048;
+// Run bounds of token t in chunk c (of C) sit at run_bound_index: blocks of
+// kRunBlock consecutive tokens per chunk, chunk after chunk, so a sorting CTA
+// (one chunk) writes whole 32-byte sectors and a dD CTA (kRunBlock
+// consecutive rows) reads its rows' bounds of every chunk as one contiguous
+// range.  Arrays hold C * round_up(total, kRunBlock) words.
+constexpr int kRunBlock = 8;
+__host__ __device__ inline int64_t run_bound_index(int64_t t, int c, int C) {
+    return ((t / kRunBlock) * C + c) * kRunBlock + (t % kRunBlock);
+}
 constexpr int kSortMaxChunks = 32;
 constexpr int kSortMaxChunkLen = 15360;   // tokens and staged output: 180 KB of shared memory
 constexpr int64_t kBackwardMaxCandidates = int64_t{kSortMaxChunks} * kSortMaxChunkLen;
+// The sort's window: 1024 tokens when documents average more than 256, else 256.
+inline bool sort_long_docs(int64_t total_tokens, int32_t n_docs) {
+    return total_tokens > 256 * static_cast<int64_t>(n_docs);
+}
 int sort_chunks(int32_t n_q, int32_t lq_max);
 cudaError_t launch_sort_and_grad_d(const BwdParams &p, cudaStream_t stream);
 // Streams `bytes` of `buf` (16-byte aligned, a multiple of 16) `passes` times

@@ -175,7 +175,9 @@ BwdLayout backward_layout(int32_t n_q, int32_t lq_max, int32_t n_docs, int64_t t
     l.col_idx = align_up(static_cast<size_t>(std::max<int64_t>(1, int64_t(n_q) * n_docs * lq_max)) * 4);
     l.doc_count = align_up(static_cast<size_t>(n_docs + 1) * 4);
     l.chunk_cnt = align_up(static_cast<size_t>(csr_chunks(n_q, lq_max, n_docs)) * std::max<int64_t>(total, 1) * 4);
-    l.row_bounds = align_up(static_cast<size_t>(sort_chunks(n_q, lq_max)) * std::max<int64_t>(total, 1) * 4);
+    // run bounds in blocks of kRunBlock tokens per chunk (run_bound_index)
+    l.row_bounds = align_up(static_cast<size_t>(sort_chunks(n_q, lq_max)) *
+                            ((std::max<int64_t>(total, 1) + kRunBlock - 1) / kRunBlock * kRunBlock) * 4);
     l.rowidx = l.col_idx;   // dQ's per-row lists of D rows: one int32 per argmax entry
     l.total = l.row_ptr + 2 * l.col_idx + l.doc_count + l.chunk_cnt + 2 * l.row_bounds + l.rowidx;
     return l;
