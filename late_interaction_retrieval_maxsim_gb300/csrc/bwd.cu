@@ -285,8 +285,12 @@ __global__ void __launch_bounds__(kCsrThreads) csr_place_kernel(BwdParams p, boo
 // warp instruction moves two rows, and the FMAs are packed two per
 // instruction: about 8 instructions per gathered row (ncu showed the
 // one-row-per-step form issuing 29 and the schedulers, not L2, setting the
-// pace).  At the end the half sums are added (half 0 + half 1).  The order is
-// fixed by the list, so the bits are the same on every run.
+// pace).  Each lane keeps four 16-byte loads in flight: the gathers are
+// bound by L2 latency, not its bandwidth (ncu: L2 throughput 35-38 %, long
+// scoreboard the top stall with two in flight; four took the training-shape
+// backward from 145 to 129 us, eight were slower).  At the end the half sums
+// are added (half 0 + half 1).  The order is fixed by the list, so the bits
+// are the same on every run.
 
 __device__ __forceinline__ uint4 load_row16(const void *base, int64_t row, int c) {
     return __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(base) + row * 256) + c);
@@ -331,12 +335,12 @@ __device__ __forceinline__ void warp_gather(const void *X, bool bf16, int n, Ent
             if (base + 32 + lane >= n) nrv = -1;
         }
         const int cnt = min(32, n - base);
-        for (int jb = 0; jb < cnt; jb += 4) {
-            int row[2];
-            float w[2];
-            uint4 raw[2];
+        for (int jb = 0; jb < cnt; jb += 8) {
+            int row[4];
+            float w[4];
+            uint4 raw[4];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
+            for (int u = 0; u < 4; ++u) {
                 const int j = jb + 2 * u + h;   // <= 31
                 row[u] = __shfl_sync(0xffffffffu, rv, j);
                 w[u] = __shfl_sync(0xffffffffu, wv, j);
@@ -344,7 +348,7 @@ __device__ __forceinline__ void warp_gather(const void *X, bool bf16, int n, Ent
                 raw[u] = row[u] >= 0 ? load_row16(X, row[u], c) : make_uint4(0u, 0u, 0u, 0u);
             }
 #pragma unroll
-            for (int u = 0; u < 2; ++u)
+            for (int u = 0; u < 4; ++u)
                 if (row[u] >= 0) fma8(raw[u], w[u], bf16, acc);
         }
         rv = nrv;
@@ -592,31 +596,20 @@ __device__ __forceinline__ int rotation(int64_t row, int n) {
 // (ascending source order, the CSR's row) as one list of n entries: lane c <
 // C holds run c's bounds, and a position maps to its run by a prefix over the
 // run lengths.  The sum visits the list from position rotation(r, n),
-// wrapping around.  A CTA's kRunBlock rows read their bounds as one
-// contiguous range, staged through shared memory.
+// wrapping around.  A CTA's kRunBlock rows share the sectors that hold
+// their bounds (run_bound_index), so its warps read them through L1.
 __global__ void __launch_bounds__(32 * kRunBlock) grad_d_kernel(BwdParams p) {
-    constexpr int kPitch = 36;   // words per row: 36 j + c spreads a 32-thread store over all banks
-    static_assert(kSortMaxChunks <= kPitch, "a row's bounds fit its pitch");
-    __shared__ int32_t s_lo[kRunBlock * kPitch], s_hi[kRunBlock * kPitch];
     const int C = p.sort_chunks;
     const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kRunBlock;
     const int64_t base = r0 * C;   // run_bound_index(r0, 0, C)
-    for (int e = threadIdx.x; e < C * kRunBlock; e += blockDim.x) {
-        const int c = e / kRunBlock, j = e - c * kRunBlock;
-        if (r0 + j < p.total_tokens) {
-            s_lo[j * kPitch + c] = __ldg(p.row_start + base + e);
-            s_hi[j * kPitch + c] = __ldg(p.row_end + base + e);
-        }
-    }
-    __syncthreads();
     const int r = static_cast<int>(r0) + (threadIdx.x >> 5);
     if (r >= p.total_tokens) return;
     const int lane = threadIdx.x & 31;
     const int wr = threadIdx.x >> 5;   // this warp's row within the block
     int lo = 0, len = 0;
     if (lane < C) {
-        lo = s_lo[wr * kPitch + lane];
-        len = s_hi[wr * kPitch + lane] - lo;
+        lo = __ldg(p.row_start + base + lane * kRunBlock + wr);
+        len = __ldg(p.row_end + base + lane * kRunBlock + wr) - lo;
     }
     int incl = len;   // inclusive prefix of the run lengths over lanes
 #pragma unroll
@@ -681,7 +674,7 @@ __global__ void __launch_bounds__(256) dq_rows_kernel(BwdParams p, int32_t *rowi
 // dQ (Eq. (2), Alg. 3 step 3): one warp owns query row (q, i) and sums
 // g[q, b] * D[rowidx[b]] over the documents, its list visited from
 // rotation(row, n_docs) upward, wrapping around.
-__global__ void __launch_bounds__(256, 8) grad_q_kernel(BwdParams p, const int32_t *rowidx) {
+__global__ void __launch_bounds__(256, 5) grad_q_kernel(BwdParams p, const int32_t *rowidx) {
     const int64_t R = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
     if (R >= static_cast<int64_t>(p.n_q) * p.lq_max) return;
     const int q = query_of(p, static_cast<int>(R));

@@ -156,7 +156,7 @@ constexpr int kSortChunkTarget = 2048;
 // Run bounds of token t in chunk c (of C) sit at run_bound_index: blocks of
 // kRunBlock consecutive tokens per chunk, chunk after chunk, so a sorting CTA
 // (one chunk) writes whole 32-byte sectors and a dD CTA (kRunBlock
-// consecutive rows) reads its rows' bounds of every chunk as one contiguous
+// consecutive rows) finds its rows' bounds of every chunk in one contiguous
 // range.  Arrays hold C * round_up(total, kRunBlock) words.
 constexpr int kRunBlock = 8;
 __host__ __device__ inline int64_t run_bound_index(int64_t t, int c, int C) {
