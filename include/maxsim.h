@@ -337,6 +337,8 @@ maxsim_status_t maxsim_build_csr(const int32_t *argmax, const int32_t *q_lens, i
  *   dD          FP32 [total_d_tokens, dim], written in full (rows nobody
  *               selected are 0).
  *   Q, D, dQ and dD must start on a 16-byte boundary.
+ * An argmax entry outside [-1, Ld_b) (of a valid query row) sets the device
+ * status word and contributes to neither gradient.
  * dtype: FP16 or BF16 (INT8 returns MAXSIM_ERR_UNSUPPORTED).  At most
  * 491,520 candidates per document (n_q * lq_max), else
  * MAXSIM_ERR_UNSUPPORTED.

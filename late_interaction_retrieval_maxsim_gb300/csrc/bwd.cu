@@ -378,15 +378,15 @@ __device__ __forceinline__ void warp_store_row(float *out_row, float2 (&acc)[4])
 // into C <= 32 chunks; one CTA per (document, chunk) keeps its chunk's
 // tokens in shared memory and sorts the chunk's sources by token with a
 // stable counting sort (per-warp histograms, a prefix over (token, warp),
-// ranks within a warp from ballots), WIN tokens at a time.  It writes the
+// ranks within a warp from lane masks), WIN tokens at a time.  It writes the
 // sorted candidates k (the source's Q row) to the fixed slots
 // [b * n_cand + k0, b * n_cand + k1) of col_idx, each source's g[q, b] to the
 // same slot of col_w, and for every token r of the document the bounds of
-// its run there to row_start / row_end at run_bound_index(r, c, C).  No prefix over documents
-// is needed, and token r's runs read chunk after chunk give its sources in
-// ascending order: the CSR's row.  (Measured alternatives: a two-pass LSD
-// radix sort on 5-bit digits was slower, 38.5 vs 23.5 us on the training
-// shape.)
+// its run there to row_start / row_end at run_bound_index(r, c, C).  No
+// prefix over documents is needed, and token r's runs read chunk after chunk
+// give its sources in ascending order: the CSR's row.  (Measured
+// alternatives: a two-pass LSD radix sort on 5-bit digits was slower, 38.5
+// vs 23.5 us on the training shape.)
 constexpr int kSortQueries = 256;   // queries of a chunk whose q_lens and g are staged
 
 // Per-warp histograms are stored with one pad word after every 32 tokens, so
@@ -436,6 +436,13 @@ __global__ void __launch_bounds__(32 * W) bwd_sort_kernel(BwdParams p) {
     static_assert((1 << KB) == WIN, "window tokens fit the key bits");
     using H = SortHist<WIN>;
     constexpr int HS = H::kStride;
+    // Ranks within a warp: at 256-token windows from per-warp lane masks in
+    // shared memory (each lane ORs its bit into its token's word, reads the
+    // word back, and the lowest lane clears it: order-free, so the same
+    // result on every run; training-shape backward 129 -> 127 us), at
+    // 1024-token windows (where the masks would cost 32 KB and a CTA per SM)
+    // from ballots.
+    constexpr bool kMaskRank = WIN == 256;
     extern __shared__ __align__(16) uint8_t ssm[];
     int32_t *tok = reinterpret_cast<int32_t *>(ssm);                 // [chunk_len]
     int32_t *hist = tok + p.sort_chunk_len;                          // [W][HS], token t at H::at(t)
@@ -443,6 +450,7 @@ __global__ void __launch_bounds__(32 * W) bwd_sort_kernel(BwdParams p) {
     int32_t *out_k = start + WIN + 1;                                // [chunk_len] the window's sorted sources
     float *out_w = reinterpret_cast<float *>(out_k + p.sort_chunk_len);   // [chunk_len] their weights
     __shared__ int32_t warp_tot[W];
+    __shared__ uint32_t s_mask[kMaskRank ? W * WIN : 1];
     __shared__ int32_t s_ql[kSortQueries];
     __shared__ float s_g[kSortQueries];
     const int C = p.sort_chunks;
@@ -465,6 +473,8 @@ __global__ void __launch_bounds__(32 * W) bwd_sort_kernel(BwdParams p) {
             s_g[qq] = p.grad[static_cast<int64_t>(q_lo + qq) * p.n_docs + b];
         }
     for (int k = threadIdx.x; k < W * HS; k += T) hist[k] = 0;
+    if constexpr (kMaskRank)
+        for (int k = threadIdx.x; k < W * WIN; k += T) s_mask[k] = 0u;
     __syncthreads();
     auto qlen_of = [&](int q) { return staged ? s_ql[q - q_lo] : p.q_lens[q]; };
     auto g_of = [&](int q) { return staged ? s_g[q - q_lo] : p.grad[static_cast<int64_t>(q) * p.n_docs + b]; };
@@ -558,7 +568,14 @@ __global__ void __launch_bounds__(32 * W) bwd_sort_kernel(BwdParams p) {
             const int kk = kb + lane;
             const int tt = kk < s_hi ? tok[kk] - w0 : -1;
             const bool mine = tt >= 0 && tt < win;
-            const unsigned peers = match_lanes<KB>(mine ? tt : 0, mine);
+            unsigned peers;
+            if constexpr (kMaskRank) {
+                if (mine) atomicOr(&s_mask[warp * WIN + tt], 1u << lane);
+                __syncwarp();
+                peers = mine ? s_mask[warp * WIN + tt] : 0u;
+            } else {
+                peers = match_lanes<KB>(mine ? tt : 0, mine);
+            }
             const int rank = __popc(peers & ((1u << lane) - 1u));
             int pos = 0;
             if (mine) pos = hist[warp * HS + H::at(tt)] + rank;
@@ -566,7 +583,10 @@ __global__ void __launch_bounds__(32 * W) bwd_sort_kernel(BwdParams p) {
             if (mine) {
                 out_k[pos] = k0 + kk;
                 out_w[pos] = g_of(query_of(p, k0 + kk));
-                if (rank == 0) hist[warp * HS + H::at(tt)] += __popc(peers);
+                if (rank == 0) {
+                    hist[warp * HS + H::at(tt)] += __popc(peers);
+                    if constexpr (kMaskRank) s_mask[warp * WIN + tt] = 0u;
+                }
             }
             __syncwarp();
         }
@@ -641,40 +661,15 @@ __global__ void __launch_bounds__(32 * kRunBlock) grad_d_kernel(BwdParams p) {
     warp_store_row(p.dD + static_cast<int64_t>(r) * 128, acc);
 }
 
-// dQ's lists: rowidx[(q * lq_max + i) * n_docs + b] = cu[b] + argmax[q, b, i]
-// (the D row query row (q, i) selected in document b), -1 for none -- the
-// argmax transposed so that a row's list is contiguous.  One CTA moves a
-// 32 x 32 tile (documents x query tokens) of one query through shared memory.
-__global__ void __launch_bounds__(256) dq_rows_kernel(BwdParams p, int32_t *rowidx) {
-    __shared__ int32_t tile[32][33];
-    const int tiles_b = (p.n_docs + 31) / 32, tiles_i = (p.lq_max + 31) / 32;
-    const int q = blockIdx.x / (tiles_b * tiles_i);
-    const int rem = blockIdx.x - q * tiles_b * tiles_i;
-    const int b0 = (rem / tiles_i) * 32, i0 = (rem % tiles_i) * 32;
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    const int qlen = p.q_lens[q];
-    for (int bb = ty; bb < 32; bb += 8) {   // read: query tokens contiguous
-        const int b = b0 + bb, i = i0 + tx;
-        int v = -1;
-        if (b < p.n_docs && i < p.lq_max && i < qlen) {
-            const int a = p.argmax[(static_cast<int64_t>(q) * p.n_docs + b) * p.lq_max + i];
-            const int lo = p.cu_seqlens[b];
-            if (a >= 0 && a < p.cu_seqlens[b + 1] - lo) v = lo + a;
-        }
-        tile[bb][tx] = v;
-    }
-    __syncthreads();
-    for (int ii = ty; ii < 32; ii += 8) {   // write: documents contiguous
-        const int b = b0 + tx, i = i0 + ii;
-        if (b < p.n_docs && i < p.lq_max)
-            rowidx[(static_cast<int64_t>(q) * p.lq_max + i) * p.n_docs + b] = tile[tx][ii];
-    }
-}
-
 // dQ (Eq. (2), Alg. 3 step 3): one warp owns query row (q, i) and sums
-// g[q, b] * D[rowidx[b]] over the documents, its list visited from
-// rotation(row, n_docs) upward, wrapping around.
-__global__ void __launch_bounds__(256, 5) grad_q_kernel(BwdParams p, const int32_t *rowidx) {
+// g[q, b] * D[cu[b] + argmax[q, b, i]] over the documents, its list visited
+// from rotation(row, n_docs) upward, wrapping around.  The argmax entries of
+// a CTA's 8 rows (consecutive i of one query) share 32-byte sectors, so its
+// warps read them through L1; an entry outside its document contributes
+// nothing (the sort reports it).  (Transposing the argmax into per-row lists
+// first, in a kernel of its own, measured slower once the gathers kept four
+// loads in flight: training-shape backward 127 -> 119 us without it.)
+__global__ void __launch_bounds__(256, 5) grad_q_kernel(BwdParams p) {
     const int64_t R = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
     if (R >= static_cast<int64_t>(p.n_q) * p.lq_max) return;
     const int q = query_of(p, static_cast<int>(R));
@@ -682,14 +677,16 @@ __global__ void __launch_bounds__(256, 5) grad_q_kernel(BwdParams p, const int32
     float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
     if (i < p.q_lens[q]) {
         const int first = rotation(R, p.n_docs);
-        const int32_t *rows = rowidx + R * p.n_docs;
+        const int32_t *am = p.argmax + static_cast<int64_t>(q) * p.n_docs * p.lq_max + i;
         const float *g = p.grad + static_cast<int64_t>(q) * p.n_docs;
         warp_gather(p.D, p.bf16 != 0, p.n_docs,
                     [&](int j, bool valid, int &row, float &w) {
                         if (!valid) return;
                         int b = j + first;
                         if (b >= p.n_docs) b -= p.n_docs;
-                        row = rows[b];
+                        const int a = __ldg(am + static_cast<int64_t>(b) * p.lq_max);
+                        const int lo = __ldg(p.cu_seqlens + b), hi = __ldg(p.cu_seqlens + b + 1);
+                        row = (a >= 0 && a < hi - lo) ? lo + a : -1;
                         w = g[b];
                     },
                     acc);
@@ -766,8 +763,8 @@ int sort_chunks(int32_t n_q, int32_t lq_max) {
 static_assert(kSortMaxChunkLen * 12 + 8 * SortHist<1024>::kStride * 4 + 1025 * 4 + 16 + 8 * kSortQueries + 64 <=
                   227 * 1024,
               "the largest sort chunk fits one CTA's shared memory (1024-token windows, 8 warps)");
-static_assert(kSortMaxChunkLen * 12 + 16 * SortHist<256>::kStride * 4 + 257 * 4 + 16 + 8 * kSortQueries + 64 <=
-                  227 * 1024,
+static_assert(kSortMaxChunkLen * 12 + 16 * SortHist<256>::kStride * 4 + 257 * 4 + 16 + 8 * kSortQueries + 64 +
+                      16 * 256 * 4 <= 227 * 1024,
               "the largest sort chunk fits one CTA's shared memory (256-token windows, 16 warps)");
 
 template <int WIN, int W>
@@ -793,16 +790,10 @@ cudaError_t launch_sort_and_grad_d(const BwdParams &p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_grad_q(const BwdParams &p, int32_t *rowidx, cudaStream_t stream) {
+cudaError_t launch_grad_q(const BwdParams &p, cudaStream_t stream) {
     const int64_t rows = static_cast<int64_t>(p.n_q) * p.lq_max;
     if (rows == 0) return cudaSuccess;
-    if (p.n_docs > 0) {
-        const int64_t tiles = static_cast<int64_t>(p.n_q) * ((p.n_docs + 31) / 32) * ((p.lq_max + 31) / 32);
-        dq_rows_kernel<<<static_cast<unsigned>(tiles), 256, 0, stream>>>(p, rowidx);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
-    grad_q_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, stream>>>(p, rowidx);
+    grad_q_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

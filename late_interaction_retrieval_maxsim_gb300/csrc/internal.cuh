@@ -143,9 +143,8 @@ int csr_chunks(int32_t n_q, int32_t lq_max, int32_t n_docs);
 constexpr int kCsrMaxDocTokens = 24 * 1024;
 // The exact CSR (maxsim_build_csr): chunked per-document counting sort.
 cudaError_t launch_build_csr(const BwdParams &p, cudaStream_t stream);
-// dQ: the argmax transposed into per-row lists of D rows (rowidx, n_q *
-// lq_max * n_docs int32 of scratch), then one warp per dQ row.
-cudaError_t launch_grad_q(const BwdParams &p, int32_t *rowidx, cudaStream_t stream);
+// dQ: one warp per dQ row, reading its argmax entries directly.
+cudaError_t launch_grad_q(const BwdParams &p, cudaStream_t stream);
 // The backward's inverse map and dD: each document's n_q * lq_max candidates
 // in C = sort_chunks() chunks (about kSortChunkTarget each, at most
 // kSortMaxChunks chunks of at most kSortMaxChunkLen), sorted per (document,

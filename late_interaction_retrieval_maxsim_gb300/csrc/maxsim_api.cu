@@ -166,7 +166,7 @@ FwdLayout forward_layout(int32_t n_q, int32_t lq_max, int32_t n_docs, maxsim_dty
 // per-(document, chunk) slots instead, with the sources' weights in a second
 // array of the same size and the runs' bounds.
 struct BwdLayout {
-    size_t row_ptr = 0, col_idx = 0, doc_count = 0, chunk_cnt = 0, row_bounds = 0, rowidx = 0, total = 0;
+    size_t row_ptr = 0, col_idx = 0, doc_count = 0, chunk_cnt = 0, row_bounds = 0, total = 0;
 };
 
 BwdLayout backward_layout(int32_t n_q, int32_t lq_max, int32_t n_docs, int64_t total) {
@@ -178,8 +178,7 @@ BwdLayout backward_layout(int32_t n_q, int32_t lq_max, int32_t n_docs, int64_t t
     // run bounds in blocks of kRunBlock tokens per chunk (run_bound_index)
     l.row_bounds = align_up(static_cast<size_t>(sort_chunks(n_q, lq_max)) *
                             ((std::max<int64_t>(total, 1) + kRunBlock - 1) / kRunBlock * kRunBlock) * 4);
-    l.rowidx = l.col_idx;   // dQ's per-row lists of D rows: one int32 per argmax entry
-    l.total = l.row_ptr + 2 * l.col_idx + l.doc_count + l.chunk_cnt + 2 * l.row_bounds + l.rowidx;
+    l.total = l.row_ptr + 2 * l.col_idx + l.doc_count + l.chunk_cnt + 2 * l.row_bounds;
     return l;
 }
 
@@ -917,7 +916,6 @@ static maxsim_status_t backward_impl(const float *grad_scores, const int32_t *ar
     p.dQ = dQ;
     p.dD = dD;
     p.bf16 = dtype == MAXSIM_BF16;
-    int32_t *rowidx = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(workspace) + l.total - l.rowidx);
     // dQ needs only the argmax: it runs on the device's side stream, forked
     // from and joined back into `stream`, while dD's (latency-bound) sort and
     // its reduction run here
@@ -926,7 +924,7 @@ static maxsim_status_t backward_impl(const float *grad_scores, const int32_t *ar
     if ((st = side_stream(&side)) != MAXSIM_OK) return st;
     cudaError_t e = cudaEventRecord(side.fork, stream);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(side.stream, side.fork, 0);
-    if (e == cudaSuccess) e = launch_grad_q(p, rowidx, side.stream);
+    if (e == cudaSuccess) e = launch_grad_q(p, side.stream);
     if (e == cudaSuccess) e = cudaEventRecord(side.join, side.stream);
     if (e != cudaSuccess) return MAXSIM_ERR_CUDA;
     e = launch_sort_and_grad_d(p, stream);

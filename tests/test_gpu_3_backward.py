@@ -177,3 +177,28 @@ def test_training_pair_names_equal_the_plain_pair(ops, case):
     else:
         Q, ql, D, cu = random_case(3, 300, [700, 64, 3, 1024], "bf16", [300, 129, 1], seed=52)
     _counted_matches_plain(ops, Q, ql, D, cu)
+
+
+def test_out_of_range_argmax_in_backward_contributes_nothing(ops):
+    """maxsim_backward with an argmax entry outside its document: the status
+    word reports it and both gradients equal the oracle's for the same
+    argmax with that entry dropped (-1)."""
+    Q, ql, D, cu = random_case(3, 8, [10, 6, 40], "bf16", [8, 5, 8], seed=71)
+    scores, argmax, _ = ops.maxsim_forward(Q, ql, D, cu)
+    g = torch.randn(scores.shape, device="cuda", generator=torch.Generator("cuda").manual_seed(9))
+    bad = argmax.clone()
+    bad[2, 1, 3] = 6           # document 1 has tokens 0..5
+    bad[0, 2, 7] = -5
+    ops.maxsim_device_status(clear=True)
+    dQ, dD = ops.maxsim_backward(g, bad, Q, ql, D, cu)
+    torch.cuda.synchronize()
+    assert ops.maxsim_device_status(clear=True) == 0x201
+    dropped = bad.clone()
+    dropped[2, 1, 3] = -1
+    dropped[0, 2, 7] = -1
+    rq, rd = oracle.backward_f64(g.double().cpu().numpy(), dropped.cpu().numpy(),
+                                 oracle.decode("bf16", syn.bits_u16(Q)), ql.cpu().numpy(),
+                                 oracle.decode("bf16", syn.bits_u16(D)), cu.cpu().numpy())
+    for got, want in ((dQ, rq), (dD, rd)):
+        assert np.abs(got.double().cpu().numpy() - want).max() <= GRAD_TOL * np.abs(want).max()
+    assert ops.maxsim_device_status() == 0
