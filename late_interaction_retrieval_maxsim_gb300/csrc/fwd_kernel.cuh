@@ -76,26 +76,32 @@ struct Cfg {
     // One or two M-tiles: two CTAs share an SM, each with half of TMEM and of
     // shared memory, so twice the epilogue warps with valid rows run per SM.
     // One M-tile: 2 slots (double-buffered), 2 document stages (INT8: one FP16
-    // stage, two INT8 staging tiles, two converter warps).  Two M-tiles
-    // (16-bit only): one slot per M-tile, one document stage, single-buffered
-    // TMEM reads (five warps per scheduler leave 96 registers).
+    // stage, two INT8 staging tiles, two converter warps); 16-bit: two
+    // epilogue warps per TMEM lane quarter, each folding half of every
+    // tile's columns (kPaired), merged per document through shared memory.
+    // Two M-tiles (16-bit only): one slot per M-tile, one document stage,
+    // single-buffered TMEM reads (five warps per scheduler leave 96
+    // registers).
     static constexpr int kCtasPerSm = (NMT == 1 || (NMT == 2 && !INT8)) ? 2 : 1;
+    static constexpr bool kPaired = NMT == 1 && !INT8;
+    static constexpr int kEpiWarps = 4 * NMT * (kPaired ? 2 : 1);
     static constexpr int kSlots = kCtasPerSm == 2 ? 2 : 4;
     static constexpr int kTmemCols = kSlots * kSlotCols;
     static constexpr int kStages = INT8 ? (NMT == 4 ? 2 : (NMT == 1 ? 1 : 3)) : (NMT == 4 ? 3 : (NMT == 1 ? 2 : 1));
     static constexpr int kI8Stages = INT8 ? (NMT == 2 ? 4 : 2) : 0;
     static constexpr int kConvWarps = INT8 ? (NMT == 2 ? 4 : 2) : 0;
-    static constexpr bool kDoubleBuffer = NMT == 1 || (NMT == 2 && INT8);
+    static constexpr bool kDoubleBuffer = INT8 && NMT <= 2;
     // A single 16-bit stage may be filled and consumed one K-block (64 of the
     // 128 dimensions) at a time (chosen per launch): the next tile's first
     // half loads while the MMAs of the second half run.
     static constexpr bool kKSplit = !INT8 && kStages == 1;
     static constexpr int kFirstEpiWarp = 2 + kConvWarps;
-    static constexpr int kThreads = 32 * (kFirstEpiWarp + 4 * NMT);
+    static constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
     static constexpr int kQBytes = NMT * kTileBytes;
     static constexpr int kDBytes = kStages * kTileBytes;
     static constexpr int kIBytes = kI8Stages * kI8TileBytes;
-    static constexpr int kSmem = 1024 + kQBytes + kDBytes + kIBytes + (int)sizeof(SharedCtl);
+    static constexpr int kPairBytes = kPaired ? 4 * (int)sizeof(PairBuf) : 0;
+    static constexpr int kSmem = 1024 + kQBytes + kDBytes + kIBytes + (int)sizeof(SharedCtl) + kPairBytes;
     static_assert(kStages >= 1 && kStages <= kMaxStages, "barrier arrays hold kMaxStages stages");
     static_assert(kI8Stages <= kMaxStages, "barrier arrays hold kMaxStages stages");
     static_assert(kSmem <= 232448, "exceeds the 227 KB shared-memory limit per CTA");
@@ -128,6 +134,7 @@ maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     uint8_t *sD = smem + C::kQBytes;
     uint8_t *sI = sD + C::kDBytes;
     SharedCtl *ctl = reinterpret_cast<SharedCtl *>(sI + C::kIBytes);
+    PairBuf *pairs = reinterpret_cast<PairBuf *>(ctl + 1);   // kPaired: one per TMEM lane quarter
     volatile int32_t *abort_flag = &ctl->abort;
 
     const int warp = threadIdx.x >> 5;
@@ -149,8 +156,10 @@ maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         }
         for (int s = 0; s < C::kSlots; ++s) {
             mbar_init(&ctl->t_full[s], 1);
-            mbar_init(&ctl->t_empty[s], 4);
+            mbar_init(&ctl->t_empty[s], 4 * (C::kPaired ? 2 : 1));
         }
+        if constexpr (C::kPaired)
+            for (int k = 0; k < 4; ++k) mbar_init(&pairs[k].bar, 2);
         mbar_init(&ctl->mma_done, 1);
         fence_mbar_init();
         ctl->abort = 0;
@@ -341,14 +350,17 @@ maxsim_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         }
     } else {
         // ------------------------------------------------ epilogue
-        const int mt = (warp - C::kFirstEpiWarp) >> 2;
+        const int e = warp - C::kFirstEpiWarp;
+        const int mt = C::kPaired ? 0 : e >> 2;
+        const int half = C::kPaired ? e >> 2 : 0;   // kPaired: which half of each tile's columns
         const int qd = warp & 3;  // TMEM lane quarter this warp may access
         if (mt < n_mt) {
-            epilogue_warp<ARGMAX, INT8 && !SCALE, SCALE, C::kDoubleBuffer>(
+            epilogue_warp<ARGMAX, INT8 && !SCALE, SCALE, C::kDoubleBuffer, C::kPaired>(
                 p, row0 + mt * 128 + qd * 32, rows_total, tmem_base, qd, b_begin, b_end, t_begin, t_end,
                 n_tiles, ctl->t_full, ctl->scale_buf[warp - C::kFirstEpiWarp],
                 [&](int j) { return make_int2(mt + NMT * (j % (C::kSlots / NMT)), j / (C::kSlots / NMT)); },
-                [&](int slot) { mbar_arrive(&ctl->t_empty[slot]); }, abort_flag);
+                [&](int slot) { mbar_arrive(&ctl->t_empty[slot]); }, abort_flag,
+                C::kPaired ? pairs + qd : nullptr, half);
         }
     }
 
