@@ -8,14 +8,20 @@
 //
 // GB300 reading of Alg. 3 step 1: every source pointing into document b lies
 // in argmax[:, b, :], so the sources are sorted document by document with a
-// stable counting sort.  A document's candidates (its n_q * lq_max argmax
-// entries in ascending flat order) are split into C contiguous chunks, one
-// CTA each: chunk histograms, a scan over documents, a per-document scan over
-// (token, chunk), then in-order placement inside each chunk (per-warp
-// histograms, a prefix over (token, warp) order, ranks from
-// __match_any_sync).  It produces exactly the global bincount / cumsum /
-// stable-argsort CSR, with no global sort; the only global atomics add
-// integer counts.
+// stable counting sort.  Two forms:
+//  * maxsim_build_csr (the exact CSR as its own entry point): a document's
+//    candidates (its n_q * lq_max argmax entries in ascending flat order)
+//    are split into C contiguous chunks, one CTA each: chunk histograms, a
+//    scan over documents, a per-document scan over (token, chunk), then
+//    in-order placement inside each chunk (per-warp histograms, a prefix
+//    over (token, warp) order, ranks from __match_any_sync).  It produces
+//    exactly the global bincount / cumsum / stable-argsort CSR, with no
+//    global sort; the only global atomics add integer counts.
+//  * maxsim_backward: one kernel sorts each (document, chunk) into fixed
+//    slots with per-(chunk, token) run bounds, needing no prefix over
+//    documents (bwd_sort_kernel); dD reads a row's runs chunk after chunk,
+//    which is its CSR row (grad_d_kernel); dQ gathers straight from the
+//    argmax (grad_q_kernel), on a second stream.
 #include "internal.cuh"
 #include "sm103.cuh"
 
