@@ -243,3 +243,58 @@ def test_argmax_exact_at_tiny_power_of_two_maxima(ops, seed):
     assert np.array_equal(ref["argmax"][:, 0], expect)           # the construction is what it claims
     assert np.array_equal(argmax[0].cpu().numpy(), ref["argmax"])
     assert np.array_equal(scores[0].double().cpu().numpy(), ref["score"])
+
+
+@pytest.mark.parametrize("n_q,lq_max", [(1, 32), (4, 8), (3, 32)])
+def test_split_column_epilogue_many_tiny_documents(ops, n_q, lq_max):
+    """Up to 128 query rows run two epilogue warps per TMEM lane quarter,
+    each folding half of every tile's columns, merged per document: 600
+    documents of 0-5 tokens (many document ends per chunk, so the merge
+    buffer fills in the middle of a chunk) plus a few long ones, every pair
+    checked; bits identical run to run."""
+    rng = np.random.default_rng(70 + n_q)
+    lengths = rng.integers(0, 6, 600).tolist()
+    lengths[100] = 300
+    lengths[400] = 129
+    q_lens = [lq_max] + rng.integers(0, lq_max + 1, n_q - 1).tolist()
+    Q, ql, D, cu = random_case(n_q, lq_max, lengths, "bf16", q_lens, seed=80 + n_q)
+    scores, argmax, _ = ops.maxsim_forward(Q, ql, D, cu)
+    assert ops.maxsim_device_status() == 0
+    check_forward("bf16", Q, ql, D, cu, scores, argmax)
+    s2, a2, _ = ops.maxsim_forward(Q, ql, D, cu)
+    assert torch.equal(scores, s2) and torch.equal(argmax, a2)
+
+
+def test_split_column_epilogue_ties_across_halves(ops):
+    """Equal maxima in both column halves of a tile (the same document token
+    repeated at columns t and t + 64): the merge keeps the lower column."""
+    rng = np.random.default_rng(13)
+    lq, ld = 32, 256
+    Qh = rng.standard_normal((lq, 128))
+    Qh /= np.linalg.norm(Qh, axis=1, keepdims=True)
+    Dh = rng.standard_normal((ld, 128))
+    Dh /= np.linalg.norm(Dh, axis=1, keepdims=True)
+    hot = rng.choice(64, lq, replace=False)
+    Dh[hot] = Qh                   # each query token's best match in the first half ...
+    Dh[hot + 64] = Qh              # ... repeated 64 columns later (second half)
+    Dh[hot + 192] = Qh             # and in the next tile's second half
+    Q = torch.tensor(Qh, dtype=torch.float16, device="cuda").view(1, lq, 128)
+    D = torch.tensor(Dh, dtype=torch.float16, device="cuda")
+    cu = torch.tensor([0, ld], dtype=torch.int32, device="cuda")
+    ql = torch.tensor([lq], dtype=torch.int32, device="cuda")
+    scores, argmax, _ = ops.maxsim_forward(Q, ql, D, cu)
+    assert ops.maxsim_device_status() == 0
+    assert np.array_equal(argmax[0, 0].cpu().numpy(), hot)
+    check_forward("fp16", Q, ql, D, cu, scores, argmax)
+
+
+def test_single_query_full_size_sampled(ops):
+    """1 query Lq=32 vs the 50,000 ColBERT documents (the single-query launch
+    the benchmark times: one M-tile, split-column epilogue); 48 sampled
+    documents."""
+    x = syn.make_inputs(syn.WORKLOADS["colbert_1q"], device="cuda")
+    scores, argmax, _ = ops.maxsim_forward(x["Q"], x["q_lens"], x["D"], x["cu_seqlens"])
+    assert ops.maxsim_device_status() == 0
+    rng = np.random.default_rng(1)
+    docs = sorted(set(rng.integers(0, 50_000, 44).tolist()) | {0, 1, 49_998, 49_999})
+    check_forward("fp16", x["Q"], x["q_lens"], x["D"], x["cu_seqlens"], scores, argmax, docs=docs)
