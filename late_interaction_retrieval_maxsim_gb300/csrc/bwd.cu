@@ -646,18 +646,21 @@ __global__ void __launch_bounds__(32 * kRunBlock) grad_d_kernel(BwdParams p) {
     const int n = __shfl_sync(0xffffffffu, incl, 31);
     const int excl = incl - len;
     const int first = rotation(r, n);
+    // the binary search's first step: the largest power of two below C
+    const int top = C > 1 ? 1 << (31 - __clz(C - 1)) : 0;
     float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
     warp_gather(p.Q, p.bf16 != 0, n,
                 [&](int j, bool valid, int &row, float &w) {
                     int pos = j + first;   // the list position visited j-th
                     if (pos >= n) pos -= n;
                     // the run holding pos: the number of runs whose end is <= pos,
-                    // found by a binary search over the lanes' inclusive ends
+                    // found by a binary search over the C lanes' inclusive ends
                     int run = 0;
 #pragma unroll
                     for (int step = 16; step > 0; step >>= 1)
-                        if (__shfl_sync(0xffffffffu, incl, run + step - 1) <= pos) run += step;
-                    run = min(run, 31);
+                        if (step <= top)   // uniform
+                            if (__shfl_sync(0xffffffffu, incl, run + step - 1) <= pos) run += step;
+                    run = min(run, C - 1);
                     const int at = __shfl_sync(0xffffffffu, lo, run) + pos - __shfl_sync(0xffffffffu, excl, run);
                     if (!valid) return;
                     row = p.col_idx[at];
