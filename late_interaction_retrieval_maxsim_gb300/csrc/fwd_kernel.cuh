@@ -106,6 +106,10 @@ struct Cfg {
     static_assert(kI8Stages <= kMaxStages, "barrier arrays hold kMaxStages stages");
     static_assert(kSmem <= 232448, "exceeds the 227 KB shared-memory limit per CTA");
     static_assert(kSlots <= kMaxSlots && kSlots % NMT == 0, "slots hold whole row groups");
+    // A paired warp may wait at a meeting while it still holds tile j's slot,
+    // and its partner may need tile j + 1 to reach the same meeting: tile
+    // j + 1 must go to another slot, or the two wait on each other.
+    static_assert(!kPaired || kSlots / NMT >= 2, "paired epilogue warps need two slots per M-tile");
     // at most kCtasPerSm CTAs fit an SM's 228 KB, so their TMEM never exceeds 512 columns
     static_assert(kCtasPerSm == 1 || 3 * (kSmem + 1024) > 233472, "a third CTA could oversubscribe TMEM");
 };
