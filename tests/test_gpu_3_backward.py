@@ -202,3 +202,20 @@ def test_out_of_range_argmax_in_backward_contributes_nothing(ops):
     for got, want in ((dQ, rq), (dD, rd)):
         assert np.abs(got.double().cpu().numpy() - want).max() <= GRAD_TOL * np.abs(want).max()
     assert ops.maxsim_device_status() == 0
+
+
+def test_colpali_training_shape_full_size(ops):
+    """64 queries x 1024 tokens vs 64 documents x 1024 tokens, BF16 (the
+    ColPali training step bench.py times): forward on sampled pairs, then
+    every dQ / dD element against the oracle, and identical bits on a
+    second backward."""
+    from maxsim_testlib import check_forward
+    x = syn.make_inputs(syn.WORKLOADS["train_colpali"], device="cuda")
+    Q, ql, D, cu = x["Q"], x["q_lens"], x["D"], x["cu_seqlens"]
+    scores, argmax, _ = ops.maxsim_forward(Q, ql, D, cu)
+    assert ops.maxsim_device_status() == 0
+    check_forward("bf16", Q, ql, D, cu, scores, argmax, pairs=[(0, 0), (5, 63), (63, 7), (31, 32)])
+    g = _contrastive_grad(scores)
+    dQ, dD = _check_backward(ops, g, argmax, Q, ql, D, cu, "bf16")
+    dQ2, dD2 = ops.maxsim_backward(g, argmax, Q, ql, D, cu)
+    assert torch.equal(dQ, dQ2) and torch.equal(dD, dD2)
