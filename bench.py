@@ -199,7 +199,9 @@ def _l2_read_gbs(m, mib=48, passes=20):
 
 
 def _extra_workloads(m, syn, rl, peaks):
-    """Shorter timings of the other workloads (median of 20 CUDA-event reps)."""
+    """Shorter timings of the other workloads: forwards as the median of 50
+    CUDA-event reps after 10 warm-up calls (p10 / p90 beside it), the rest of
+    20."""
     import torch
     out = {}
     stream = torch.cuda.current_stream()
@@ -217,8 +219,9 @@ def _extra_workloads(m, syn, rl, peaks):
         ws = torch.empty(max(1, m.maxsim_forward_workspace_size(w.n_q, w.lq, w.n_docs, w.dtype)),
                          dtype=torch.uint8, device="cuda")
         _, per = _time_loop(lambda: m.maxsim_forward(Q, ql, D, cu, scores=s, argmax=a, workspace=ws,
-                                                     **kw), 20, 3, stream)
+                                                     **kw), 50, 10, stream)
         ms = statistics.median(per)
+        dec = statistics.quantiles(per, n=10)   # deciles: p10 .. p90
         # device memory held by one forward: inputs, outputs and workspace
         # (the similarity tensor is never materialised; its FP32 size for
         # comparison)
@@ -227,7 +230,8 @@ def _extra_workloads(m, syn, rl, peaks):
                                                        **kw), 20, 3, stream)
         flops = rl.forward_flops(int(ql.sum()), D.shape[0])
         rec = {"n_q": w.n_q, "lq": w.lq, "n_docs": w.n_docs, "ld": [w.ld_lo, w.ld_hi],
-               "dtype": w.dtype, "fwd_ms": round(ms, 4), "docs_per_s": w.n_docs / (ms / 1e3),
+               "dtype": w.dtype, "fwd_ms": round(ms, 4), "fwd_p10_ms": round(dec[0], 4),
+               "fwd_p90_ms": round(dec[-1], 4), "docs_per_s": w.n_docs / (ms / 1e3),
                "fwd_tflops": flops / (ms / 1e3) / 1e12,
                "fwd_frac_of_measured_bf16_peak": flops / (ms / 1e3) / 1e12 / peaks["bf16_tflops"],
                "fwd_value_only_ms": round(statistics.median(per_v), 4),
@@ -249,8 +253,9 @@ def _extra_workloads(m, syn, rl, peaks):
                               dtype=torch.uint8, device="cuda")
             dq, dd = m.maxsim_backward(g, a, Q, ql, D, cu, workspace=bws)
             _, perb = _time_loop(lambda: m.maxsim_backward(g, a, Q, ql, D, cu, dQ=dq, dD=dd,
-                                                           workspace=bws), 20, 3, stream)
+                                                           workspace=bws), 50, 10, stream)
             msb = statistics.median(perb)
+            decb = statistics.quantiles(perb, n=10)
 
             # one training step, forward then backward, on resident inputs
             def train_step():
@@ -283,7 +288,8 @@ def _extra_workloads(m, syn, rl, peaks):
             bb = rl.backward_hbm_bytes(w.n_q, w.lq, w.n_docs, D.shape[0], int(ql.sum()) * w.n_docs)
             n_src = int(ql.sum()) * w.n_docs
             gather = 2 * n_src * w.dim * 2
-            rec.update(bwd_ms=round(msb, 4), step_ms=round(ms + msb, 4),
+            rec.update(bwd_ms=round(msb, 4), bwd_p10_ms=round(decb[0], 4), bwd_p90_ms=round(decb[-1], 4),
+                       step_ms=round(ms + msb, 4),
                        bwd_algorithmic_bytes=bb["total"],
                        bwd_l2_gather_bytes=gather,
                        bwd_gbs=bb["total"] / (msb / 1e3) / 1e9,
