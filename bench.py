@@ -232,6 +232,8 @@ def _extra_workloads(m, syn, rl, peaks):
         rec = {"n_q": w.n_q, "lq": w.lq, "n_docs": w.n_docs, "ld": [w.ld_lo, w.ld_hi],
                "dtype": w.dtype, "fwd_ms": round(ms, 4), "fwd_p10_ms": round(dec[0], 4),
                "fwd_p90_ms": round(dec[-1], 4), "docs_per_s": w.n_docs / (ms / 1e3),
+               # query-token x document-token similarities formed (and folded) per second
+               "token_pairs_per_s": int(ql.sum()) * D.shape[0] / (ms / 1e3),
                "fwd_tflops": flops / (ms / 1e3) / 1e12,
                "fwd_frac_of_measured_bf16_peak": flops / (ms / 1e3) / 1e12 / peaks["bf16_tflops"],
                "fwd_value_only_ms": round(statistics.median(per_v), 4),
