@@ -487,8 +487,40 @@ __global__ void __launch_bounds__(32 * W) bwd_sort_kernel(BwdParams p) {
 
     const int seg = ((len + W - 1) / W + 31) / 32 * 32;
     const int s_lo = min(len, warp * seg), s_hi = min(len, s_lo + seg);
-    // 1. the warp's segment: the token each candidate names, or -1 (four loads
-    //    in flight per lane), counted at once for the first window
+    // 1. the warp's segment: the token each candidate names, or -1, counted at
+    //    once for the first window.  With lq_max and k0 multiples of 4 and a
+    //    16-byte aligned argmax, a lane loads four consecutive candidates (one
+    //    query row, 16 bytes) at once; otherwise four loads at stride 32.
+    auto record = [&](int kk, int v) {
+        if (v < -1 || v >= ld) {
+            atomicCAS(p.status, 0, ptx::kStatusBadArgmax);
+            v = -1;
+        }
+        tok[kk] = v;
+        if (v >= 0 && v < WIN) atomicAdd(&hist[warp * HS + H::at(v)], 1);
+    };
+    const bool vec = (p.lq_max & 3) == 0 && (k0 & 3) == 0 && (reinterpret_cast<uintptr_t>(p.argmax) & 15) == 0;
+    if (vec)
+        for (int kb = s_lo + 4 * lane; kb < s_hi; kb += 4 * 32) {
+            const int k = k0 + kb;
+            const int q = query_of(p, k);
+            const int i = k - q * p.lq_max;
+            const int32_t *src = p.argmax + (static_cast<int64_t>(q) * p.n_docs + b) * p.lq_max + i;
+            int4 a4 = make_int4(-1, -1, -1, -1);
+            if (kb + 3 < s_hi) {
+                a4 = *reinterpret_cast<const int4 *>(src);
+            } else {
+                a4.x = src[0];
+                if (kb + 1 < s_hi) a4.y = src[1];
+                if (kb + 2 < s_hi) a4.z = src[2];
+            }
+            const int ql = qlen_of(q);
+            const int av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (kb + u < s_hi) record(kb + u, i + u < ql ? av[u] : -1);
+        }
+    else
     for (int kb = s_lo + lane; kb < s_hi; kb += 4 * 32) {
         int a[4];
 #pragma unroll
@@ -505,14 +537,7 @@ __global__ void __launch_bounds__(32 * W) bwd_sort_kernel(BwdParams p) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int kk = kb + 32 * u;
-            if (kk >= s_hi) continue;
-            int v = a[u];
-            if (v < -1 || v >= ld) {
-                atomicCAS(p.status, 0, ptx::kStatusBadArgmax);
-                v = -1;
-            }
-            tok[kk] = v;
-            if (v >= 0 && v < WIN) atomicAdd(&hist[warp * HS + H::at(v)], 1);
+            if (kk < s_hi) record(kk, a[u]);
         }
     }
     int32_t win_base = b * n_cand + k0;   // first slot of the current window's sources (< 2^31)

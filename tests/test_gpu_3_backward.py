@@ -219,3 +219,23 @@ def test_colpali_training_shape_full_size(ops):
     dQ, dD = _check_backward(ops, g, argmax, Q, ql, D, cu, "bf16")
     dQ2, dD2 = ops.maxsim_backward(g, argmax, Q, ql, D, cu)
     assert torch.equal(dQ, dQ2) and torch.equal(dD, dD2)
+
+
+@pytest.mark.parametrize("case", ["odd_lq", "unaligned_argmax"])
+def test_sort_scalar_argmax_loads(ops, case):
+    """The sort loads four argmax entries at once only when lq_max is a
+    multiple of 4 and the argmax is 16-byte aligned: an odd lq_max, and an
+    argmax view that starts 4 bytes into its buffer, take the one-entry path
+    and give the same gradients as the oracle."""
+    lq = 7 if case == "odd_lq" else 8
+    Q, ql, D, cu = random_case(5, lq, [40, 3, 0, 130, 17], "fp16", [lq, 1, lq - 2, 0, lq], seed=77)
+    scores, argmax, _ = ops.maxsim_forward(Q, ql, D, cu)
+    if case == "unaligned_argmax":
+        buf = torch.empty(argmax.numel() + 1, dtype=torch.int32, device="cuda")
+        view = buf[1:].view(argmax.shape)
+        view.copy_(argmax)
+        assert view.data_ptr() % 16 != 0
+        argmax = view
+    g = torch.randn(scores.shape, device="cuda", generator=torch.Generator("cuda").manual_seed(12))
+    _check_csr(ops, argmax.contiguous(), ql, cu, D.shape[0])
+    _check_backward(ops, g, argmax, Q, ql, D, cu, "fp16")
