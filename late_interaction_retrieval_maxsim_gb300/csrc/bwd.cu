@@ -429,9 +429,10 @@ __device__ __forceinline__ unsigned match_lanes(int key, bool valid) {
 // use 16 warps; the 1024-token histograms leave room for 8.
 template <int WIN, int W>
 size_t sort_smem_bytes(int chunk_len) {
-    // tokens, per-warp histograms, run starts, and the window's sorted output
-    // (candidate and weight) staged for coalesced writes
-    return static_cast<size_t>(chunk_len) * 4 * 3 + W * SortHist<WIN>::kStride * 4 + (WIN + 1) * 4 + 16;
+    // tokens, per-warp histograms, run starts, and the window's sorted
+    // candidates staged for coalesced writes (their weights are looked up as
+    // they are written: staging them too cost the 256-token form a CTA per SM)
+    return static_cast<size_t>(chunk_len) * 4 * 2 + W * SortHist<WIN>::kStride * 4 + (WIN + 1) * 4 + 16;
 }
 
 template <int WIN, int W>
@@ -454,7 +455,6 @@ __global__ void __launch_bounds__(32 * W) bwd_sort_kernel(BwdParams p) {
     int32_t *hist = tok + p.sort_chunk_len;                          // [W][HS], token t at H::at(t)
     int32_t *start = hist + W * HS;                                  // [WIN + 1]
     int32_t *out_k = start + WIN + 1;                                // [chunk_len] the window's sorted sources
-    float *out_w = reinterpret_cast<float *>(out_k + p.sort_chunk_len);   // [chunk_len] their weights
     __shared__ int32_t warp_tot[W];
     __shared__ uint32_t s_mask[kMaskRank ? W * WIN : 1];
     __shared__ int32_t s_ql[kSortQueries];
@@ -613,7 +613,6 @@ __global__ void __launch_bounds__(32 * W) bwd_sort_kernel(BwdParams p) {
             __syncwarp();
             if (mine) {
                 out_k[pos] = k0 + kk;
-                out_w[pos] = g_of(query_of(p, k0 + kk));
                 if (rank == 0) {
                     hist[warp * HS + H::at(tt)] += __popc(peers);
                     if constexpr (kMaskRank) s_mask[warp * WIN + tt] = 0u;
@@ -625,8 +624,9 @@ __global__ void __launch_bounds__(32 * W) bwd_sort_kernel(BwdParams p) {
         // 5. the window's sorted sources to their slots, coalesced
         const int n_win = start[WIN];
         for (int e = threadIdx.x; e < n_win; e += T) {
-            p.col_idx[win_base + e] = out_k[e];
-            p.col_w[win_base + e] = out_w[e];
+            const int k = out_k[e];
+            p.col_idx[win_base + e] = k;
+            p.col_w[win_base + e] = g_of(query_of(p, k));
         }
         win_base += n_win;
         __syncthreads();
@@ -794,10 +794,10 @@ int sort_chunks(int32_t n_q, int32_t lq_max) {
     return static_cast<int>(c < 1 ? 1 : (c > kSortMaxChunks ? kSortMaxChunks : c));
 }
 
-static_assert(kSortMaxChunkLen * 12 + 8 * SortHist<1024>::kStride * 4 + 1025 * 4 + 16 + 8 * kSortQueries + 64 <=
+static_assert(kSortMaxChunkLen * 8 + 8 * SortHist<1024>::kStride * 4 + 1025 * 4 + 16 + 8 * kSortQueries + 64 <=
                   227 * 1024,
               "the largest sort chunk fits one CTA's shared memory (1024-token windows, 8 warps)");
-static_assert(kSortMaxChunkLen * 12 + 16 * SortHist<256>::kStride * 4 + 257 * 4 + 16 + 8 * kSortQueries + 64 +
+static_assert(kSortMaxChunkLen * 8 + 16 * SortHist<256>::kStride * 4 + 257 * 4 + 16 + 8 * kSortQueries + 64 +
                       16 * 256 * 4 <= 227 * 1024,
               "the largest sort chunk fits one CTA's shared memory (256-token windows, 16 warps)");
 

@@ -162,7 +162,7 @@ __host__ __device__ inline int64_t run_bound_index(int64_t t, int c, int C) {
     return ((t / kRunBlock) * C + c) * kRunBlock + (t % kRunBlock);
 }
 constexpr int kSortMaxChunks = 32;
-constexpr int kSortMaxChunkLen = 15360;   // tokens and staged output: 180 KB of shared memory
+constexpr int kSortMaxChunkLen = 15360;   // tokens and staged output: 120 KB of shared memory
 constexpr int64_t kBackwardMaxCandidates = int64_t{kSortMaxChunks} * kSortMaxChunkLen;
 // The sort's window: 1024 tokens when documents average more than 256, else 256.
 inline bool sort_long_docs(int64_t total_tokens, int32_t n_docs) {
