@@ -20,7 +20,9 @@
 //  * tcgen05.mma (M=128, N=128 tokens, K=16, FP32 accumulate) writes
 //    similarity tiles into TMEM accumulator slots of 128 columns (4 per SM),
 //    which the MMA fills while the epilogue drains the others.
-//  * Epilogue warps (one warp-set of 4 per M-tile, one thread per query row)
+//  * Epilogue warps (one warp-set of 4 per M-tile, one thread per query row;
+//    a single 16-bit M-tile gets two sets, each folding half of every tile's
+//    columns, their per-document results merged through shared memory)
 //    read TMEM with tcgen05.ld and fold each 32-column chunk into the row's
 //    running (max, argmax) with a balanced comparison tree (ties keep the
 //    lowest token), splitting chunks at document boundaries; at a document's
